@@ -1,0 +1,300 @@
+"""Plain fp64 CPU oracle for the Wan2.2 VAE-decoder causal-convolution stack.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports this module:
+only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may call it. It shares no code with the CUDA path.
+
+Every function takes numpy arrays (any float dtype; they are widened to
+float64), applies no intermediate rounding and returns float64. Activations
+are channels-last: ``[N, D, H, W, C]``. Weights keep the PyTorch Conv3d
+order ``[C_out, C_in, kt, kh, kw]``.
+
+Sources (pages of the reference material, by title and item):
+
+* "FastVideo wan22_vae_decode solution/attn.cu", header comment: one head of
+  softmax(q k^T / 32) v per latent frame over H*W positions, C=1024, no mask;
+  the host code computes the scale as 1/sqrt(C) and the GEMM problem is a
+  cross-correlation (no kernel flip).
+* "FastVideo wan22_vae_decode solution/resample.h", header comment: the
+  resampler is nearest x2 in space followed by a 3x3x3 convolution; bias and
+  the nearest-duplicated shortcut are added after the convolution. The
+  comment on ``resample_upsample``: the input carries two causal history
+  frames in time and one row of zero padding.
+* "FastVideo wan22_vae_decode solution/head.cu", header comment and
+  ``head_stencil_kernel``: conv_out to 12 channels, bias, clamp to [-1, 1],
+  zero padding in the plane; the two-stage split (temporal 3x1x1 conv into
+  9x12 channels, then a 3x3 spatial sum) is the same sum regrouped.
+* The benchmark spec of this stack: causal 3x3x3 convolution with two history
+  frames (zeros before frame 0) and spatial zero padding of 1.
+
+Readings where the pages are silent (each one is listed with its reason in the
+design notes of the repository):
+
+* Temporal alignment: tap kt reads frame t + kt - 2 (causal front padding of
+  two frames); kh, kw read h + kh - 1, w + kw - 1.
+* The resampler's shortcut has the input's channel count and is duplicated
+  x2 in space only (no temporal duplication, no channel-to-row rearrangement).
+* Attention normalises over keys (rows of P sum to one).
+* The clamp is applied after the bias, to the closed interval [-1, 1].
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "causal_conv3d",
+    "causal_conv3d_at",
+    "nearest_up2",
+    "resample_up2",
+    "resample_up2_at",
+    "resample_phase_kernels",
+    "resample_up2_four_phase",
+    "attn_probs",
+    "attn_frame",
+    "attn_frame_rows",
+    "head_out",
+    "head_out_at",
+    "head_two_stage",
+]
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def _pad_causal(x: np.ndarray, history: np.ndarray | None) -> np.ndarray:
+    """x [N,D,H,W,C] -> [N,D+2,H+2,W+2,C]: two frames in front (zeros, or the
+    given history), one zero row/column on each side in the plane."""
+    n, d, h, w, c = x.shape
+    xp = np.zeros((n, d + 2, h + 2, w + 2, c), dtype=np.float64)
+    xp[:, 2:, 1:-1, 1:-1, :] = x
+    if history is not None:
+        hist = _f64(history)
+        assert hist.shape == (n, 2, h, w, c), hist.shape
+        xp[:, :2, 1:-1, 1:-1, :] = hist
+    return xp
+
+
+def causal_conv3d(x, w, b=None, history=None) -> np.ndarray:
+    """Causal 3x3x3 convolution, the plain definition.
+
+    y[n,t,h,w,co] = b[co] + sum_{ci,kt,kh,kw} w[co,ci,kt,kh,kw]
+                                  * x~[n, t+kt-2, h+kh-1, w+kw-1, ci]
+
+    with x~ = 0 outside the plane and, before frame 0, either zeros
+    (``history=None``) or the two given history frames ``[N,2,H,W,Cin]``.
+    Cross-correlation (no flip), as the attention page's GEMM problem states
+    for the same convolution machinery.
+    """
+    x = _f64(x)
+    w = _f64(w)
+    n, d, h, wd, cin = x.shape
+    cout = w.shape[0]
+    assert w.shape == (cout, cin, 3, 3, 3), w.shape
+    xp = _pad_causal(x, history)
+    y = np.zeros((n, d, h, wd, cout), dtype=np.float64)
+    if b is not None:
+        y += _f64(b)
+    for kt in range(3):
+        for kh in range(3):
+            for kw in range(3):
+                # the channel sum of one tap, as a matrix product
+                y += xp[:, kt:kt + d, kh:kh + h, kw:kw + wd, :] @ w[:, :, kt, kh, kw].T
+    return y
+
+
+def causal_conv3d_at(x, w, b, points, history=None) -> np.ndarray:
+    """The same convolution evaluated only at ``points`` (an int array [P,4]
+    of (n, t, h, w)); returns [P, Cout]. Used where the full output is too
+    large for the CPU."""
+    x = _f64(x) if x.dtype != np.float64 else x
+    w = _f64(w)
+    pts = np.asarray(points, dtype=np.int64).reshape(-1, 4)
+    n, d, h, wd, cin = x.shape
+    cout = w.shape[0]
+    out = np.zeros((len(pts), cout), dtype=np.float64)
+    if b is not None:
+        out += _f64(b)
+    hist = None if history is None else _f64(history)
+    for kt in range(3):
+        for kh in range(3):
+            for kw in range(3):
+                tt = pts[:, 1] + kt - 2
+                hh = pts[:, 2] + kh - 1
+                ww = pts[:, 3] + kw - 1
+                inside = (hh >= 0) & (hh < h) & (ww >= 0) & (ww < wd)
+                win = np.zeros((len(pts), cin), dtype=np.float64)
+                cur = inside & (tt >= 0)
+                win[cur] = x[pts[cur, 0], tt[cur], hh[cur], ww[cur], :]
+                if hist is not None:
+                    old = inside & (tt < 0)
+                    win[old] = hist[pts[old, 0], tt[old] + 2, hh[old], ww[old], :]
+                out += win @ w[:, :, kt, kh, kw].T
+    return out
+
+
+def nearest_up2(x) -> np.ndarray:
+    """Nearest-neighbour x2 in space: u[n,t,y,x,c] = x[n,t,y//2,x//2,c]."""
+    x = _f64(x)
+    return np.repeat(np.repeat(x, 2, axis=2), 2, axis=3)
+
+
+def resample_up2(x, w, b, skip, history=None) -> np.ndarray:
+    """Spatial resampler, direct form: nearest x2 in space, the causal 3x3x3
+    convolution with bias, then the nearest-duplicated shortcut added."""
+    hist_up = None if history is None else nearest_up2(history)
+    return causal_conv3d(nearest_up2(x), w, b, hist_up) + nearest_up2(skip)
+
+
+def resample_up2_at(x, w, b, skip, points, history=None) -> np.ndarray:
+    """The direct resampler at high-resolution ``points`` [P,4] of
+    (n, t, y, x); the up-sampled tensor is indexed, never materialised."""
+    x = _f64(x) if x.dtype != np.float64 else x
+    w = _f64(w)
+    pts = np.asarray(points, dtype=np.int64).reshape(-1, 4)
+    n, d, hl, wl, cin = x.shape
+    hh_max, ww_max = 2 * hl, 2 * wl
+    cout = w.shape[0]
+    out = np.zeros((len(pts), cout), dtype=np.float64) + _f64(b)
+    hist = None if history is None else _f64(history)
+    for kt in range(3):
+        for kh in range(3):
+            for kw in range(3):
+                tt = pts[:, 1] + kt - 2
+                yy = pts[:, 2] + kh - 1
+                xx = pts[:, 3] + kw - 1
+                inside = (yy >= 0) & (yy < hh_max) & (xx >= 0) & (xx < ww_max)
+                win = np.zeros((len(pts), cin), dtype=np.float64)
+                cur = inside & (tt >= 0)
+                win[cur] = x[pts[cur, 0], tt[cur], yy[cur] // 2, xx[cur] // 2, :]
+                if hist is not None:
+                    old = inside & (tt < 0)
+                    win[old] = hist[pts[old, 0], tt[old] + 2, yy[old] // 2, xx[old] // 2, :]
+                out += win @ w[:, :, kt, kh, kw].T
+    s = skip if skip.dtype == np.float64 else _f64(skip)
+    out += s[pts[:, 0], pts[:, 1], pts[:, 2] // 2, pts[:, 3] // 2, :]
+    return out
+
+
+# Rows of the 3x3 kernel that land on low-resolution row i + p - 1 + a, for
+# output parity p and phase tap a (nearest x2 maps rows 2i+p-1..2i+p+1 onto
+# low-resolution rows i-1, i, i+1).
+_PHASE_ROWS = {(0, 0): (0,), (0, 1): (1, 2), (1, 0): (0, 1), (1, 1): (2,)}
+
+
+def resample_phase_kernels(w) -> np.ndarray:
+    """The four per-phase 3x2x2 kernels with repeated taps summed.
+
+    Returns pk[2p+q, co, ci, kt, a, b] (fp64). The decomposition the
+    resample.h header describes: nearest x2 then 3x3x3 equals one low-resolution
+    conv per output parity (p, q) whose taps are sums of the original taps.
+    """
+    w = _f64(w)
+    cout, cin = w.shape[:2]
+    pk = np.zeros((4, cout, cin, 3, 2, 2), dtype=np.float64)
+    for p in range(2):
+        for q in range(2):
+            for a in range(2):
+                for bb in range(2):
+                    for kh in _PHASE_ROWS[(p, a)]:
+                        for kw in _PHASE_ROWS[(q, bb)]:
+                            pk[2 * p + q, :, :, :, a, bb] += w[:, :, :, kh, kw]
+    return pk
+
+
+def resample_up2_four_phase(x, w, b, skip) -> np.ndarray:
+    """The resampler through the four-phase form, kept only to check the
+    decomposition against the direct form: each phase is a causal 3x2x2 conv
+    at low resolution, reading x~[t+kt-2, i+p-1+a, j+q-1+b]; the interleave
+    then writes out[t, 2i+p, 2j+q] = phase + bias + skip."""
+    x = _f64(x)
+    n, d, hl, wl, cin = x.shape
+    pk = resample_phase_kernels(w)
+    cout = pk.shape[1]
+    xp = _pad_causal(x, None)  # index offset: frame +2, row +1, column +1
+    out = np.zeros((n, d, 2 * hl, 2 * wl, cout), dtype=np.float64)
+    s = _f64(skip)
+    for p in range(2):
+        for q in range(2):
+            ph = np.zeros((n, d, hl, wl, cout), dtype=np.float64)
+            for kt in range(3):
+                for a in range(2):
+                    for bb in range(2):
+                        r0 = p + a  # = (i + p - 1 + a) + 1 - i
+                        c0 = q + bb
+                        ph += xp[:, kt:kt + d, r0:r0 + hl, c0:c0 + wl, :] @ pk[2 * p + q, :, :, kt, a, bb].T
+            out[:, :, p::2, q::2, :] = ph + _f64(b) + s
+    return out
+
+
+def attn_probs(q, k, scale=None) -> np.ndarray:
+    """P = softmax over keys of (q k^T) * scale, per frame; q,k [T,HW,C].
+    The maximum is subtracted before the exponential (attn.cu, stage 3)."""
+    q = _f64(q)
+    k = _f64(k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(q.shape[-1])
+    s = np.einsum("tic,tjc->tij", q, k) * scale
+    s -= s.max(axis=-1, keepdims=True)
+    e = np.exp(s)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def attn_frame(q, k, v, scale=None) -> np.ndarray:
+    """Single-head attention per latent frame, no mask: O = softmax(q k^T *
+    scale) v with scale = 1/sqrt(C) by default. q, k, v [T, HW, C]."""
+    p = attn_probs(q, k, scale)
+    return np.einsum("tij,tjc->tic", p, _f64(v))
+
+
+def attn_frame_rows(q, k, v, rows, scale=None) -> np.ndarray:
+    """Attention output for the query rows ``rows`` [P,2] of (frame, i)."""
+    q = _f64(q) if q.dtype != np.float64 else q
+    k = _f64(k) if k.dtype != np.float64 else k
+    v = _f64(v) if v.dtype != np.float64 else v
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1, 2)
+    if scale is None:
+        scale = 1.0 / np.sqrt(q.shape[-1])
+    out = np.zeros((len(rows), v.shape[-1]), dtype=np.float64)
+    for idx, (t, i) in enumerate(rows):
+        s = (k[t] @ q[t, i]) * scale
+        e = np.exp(s - s.max())
+        out[idx] = (e / e.sum()) @ v[t]
+    return out
+
+
+def head_out(x, w, b, history=None) -> np.ndarray:
+    """Output head: causal conv_out (3x3x3, C_in -> 12), bias, clamp to [-1, 1]."""
+    return np.clip(causal_conv3d(x, w, b, history), -1.0, 1.0)
+
+
+def head_out_at(x, w, b, points, history=None) -> np.ndarray:
+    """The head at ``points`` [P,4] of (n, t, h, w)."""
+    return np.clip(causal_conv3d_at(x, w, b, points, history), -1.0, 1.0)
+
+
+def head_two_stage(x, w, b) -> np.ndarray:
+    """The head regrouped as on the head.cu page, kept only to check that the
+    regrouping is the same sum: stage A is a temporal-only (3x1x1) conv whose
+    output channel (i*3+j)*12 + c holds spatial tap (i, j) of channel c; stage B
+    sums, at each position, tap (i, j) read from position (h+i-1, w+j-1)
+    (zero outside the plane), adds the bias and clamps."""
+    x = _f64(x)
+    w = _f64(w)
+    n, d, h, wd, cin = x.shape
+    cout = w.shape[0]
+    xp = np.zeros((n, d + 2, h, wd, cin), dtype=np.float64)
+    xp[:, 2:] = x
+    g = np.zeros((n, d, h, wd, 9 * cout), dtype=np.float64)
+    for i in range(3):
+        for j in range(3):
+            for kt in range(3):
+                g[..., (i * 3 + j) * cout:(i * 3 + j + 1) * cout] += xp[:, kt:kt + d] @ w[:, :, kt, i, j].T
+    gp = np.zeros((n, d, h + 2, wd + 2, 9 * cout), dtype=np.float64)
+    gp[:, :, 1:-1, 1:-1] = g
+    y = np.zeros((n, d, h, wd, cout), dtype=np.float64) + _f64(b)
+    for i in range(3):
+        for j in range(3):
+            y += gp[:, :, i:i + h, j:j + wd, (i * 3 + j) * cout:(i * 3 + j + 1) * cout]
+    return np.clip(y, -1.0, 1.0)
