@@ -1,0 +1,506 @@
+"""Benchmark of the causal-convolution stack on GB300.
+
+One step = one 4-latent-frame chunk through all four stages of the hot path
+at the configured sizes, every kernel launched through the C ABI:
+
+  mid-block causal conv 1024->1024 @ 4x44x78          (1 launch)
+  attention, 4 frames x 3432 positions x C=1024       (scores, softmax, PV)
+  resampler 512->512 @ 8x88x156 -> 8x176x312          (phase convs, interleave)
+  output head 256->12 @ 16x352x624                    (temporal conv, stencil)
+
+`value` is milliseconds per chunk for the whole job (with N GPUs each rank
+decodes its own chunk: value = max-over-ranks step time / N). Inputs are
+synthetic (seeded), resident in HBM; the per-step working set (~4.3 GB) is
+far larger than L2, so every step's reads come from DRAM (no explicit flush).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from causal_convolution_gb300 import inputs as cc_inputs  # noqa: E402
+
+METRIC = "causal-conv TFLOP/s (% of bf16 peak); resampler HBM GB/s; ms per 4-frame chunk"
+WORKLOAD = ("one 4-latent-frame chunk through the four stages: causal conv 1024->1024 @ 4x44x78; "
+            "attention 4x3432xC1024; resampler 512->512 @ 8x88x156 -> 8x176x312; head 256->12 @ 16x352x624")
+
+KERNELS = ["conv3d_causal", "attn_scores", "attn_softmax", "attn_pv", "resample_phase_conv",
+           "resample_interleave", "head_temporal", "head_stencil"]
+
+
+def algorithmic_work():
+    """Per-launch algorithmic work of every kernel: (bound, amount, unit)."""
+    cv = cc_inputs.CONFIGS["mid_conv"]
+    at = cc_inputs.CONFIGS["attention"]
+    rs = cc_inputs.CONFIGS["resampler"]
+    hd = cc_inputs.CONFIGS["head"]
+    m_conv = cv.n * cv.d * cv.h * cv.w
+    m_res = rs.n * rs.d * rs.h * rs.w
+    m_head = hd.n * hd.d * hd.h * hd.w
+    t, hw, c = at.d, at.hw, at.c
+    ld = (hw + 7) // 8 * 8
+    return {
+        "conv3d_causal": ("tensor", 2.0 * m_conv * cv.cout * 27 * cv.c, "flop"),
+        "attn_scores": ("tensor", 2.0 * t * hw * hw * c, "flop"),
+        "attn_softmax": ("hbm", t * hw * hw * 4.0 + t * hw * ld * 2.0, "byte"),
+        "attn_pv": ("tensor", 2.0 * t * hw * hw * c, "flop"),
+        "resample_phase_conv": ("tensor", 2.0 * 4 * m_res * rs.cout * 12 * rs.c, "flop"),
+        "resample_interleave": ("hbm", (4 + 1 + 4) * m_res * rs.c * 2.0, "byte"),
+        "head_temporal": ("hbm", m_head * hd.c * 2.0 + m_head * 112 * 2.0, "byte"),
+        "head_stencil": ("hbm", m_head * 112 * 2.0 + m_head * 12 * 2.0, "byte"),
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of this GPU while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            try:
+                sm.append(float(s[0]))
+                mx.append(float(s[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, s[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload --
+
+class Workload:
+    """All inputs, prepared weights, workspaces and outputs of one chunk, on one GPU."""
+
+    def __init__(self, device):
+        from causal_convolution_gb300 import api
+        self.api = api
+        self.dev = device
+        bf = torch.bfloat16
+        E = lambda *s, dt=bf: torch.empty(s, dtype=dt, device=device)
+        mk = cc_inputs.make_config_inputs
+
+        cv = cc_inputs.CONFIGS["mid_conv"]
+        i = mk("mid_conv", device)
+        self.cv = cv
+        self.conv_x, self.conv_b = i["x"], i["b"]
+        self.conv_wp = E(27 * cv.cout * cv.c)
+        api.cc_conv3d_prepare(i["w"], self.conv_wp)
+        self.conv_y = E(cv.n, cv.d, cv.h, cv.w, cv.cout)
+
+        at = cc_inputs.CONFIGS["attention"]
+        i = mk("attention", device)
+        self.at = at
+        self.q, self.k, self.v = i["q"], i["k"], i["v"]
+        self.ld = api.cc_attn_ld(at.hw)
+        self.s = E(at.d, at.hw, self.ld, dt=torch.float32)
+        self.p = E(at.d, at.hw, self.ld)
+        self.o = E(at.d, at.hw, at.c)
+        self.scale = at.c ** -0.5
+
+        rs = cc_inputs.CONFIGS["resampler"]
+        i = mk("resampler", device)
+        self.rs = rs
+        self.res_x, self.res_b, self.res_skip = i["x"], i["b"], i["skip"]
+        self.res_pw = E(48 * rs.cout * rs.c)
+        api.cc_resample_prepare(i["w"], self.res_pw)
+        self.phases = E(4, rs.n, rs.d, rs.h, rs.w, rs.cout)
+        self.res_out = E(rs.n, rs.d, 2 * rs.h, 2 * rs.w, rs.cout)
+
+        hd = cc_inputs.CONFIGS["head"]
+        i = mk("head", device)
+        self.hd = hd
+        self.head_x, self.head_b = i["x"], i["b"]
+        self.head_wp = E(3 * api.HEAD_G_CH * hd.c)
+        api.cc_head_prepare(i["w"], self.head_wp)
+        self.g = E(hd.n, hd.d, hd.h, hd.w, api.HEAD_G_CH)
+        self.head_out = E(hd.n, hd.d, hd.h, hd.w, api.HEAD_COUT)
+        torch.cuda.synchronize(device)
+        api.cc_check_device()
+
+    def step(self, stream, ev=None):
+        """The whole hot path once. With `ev` (9 events) each launch is bracketed."""
+        a = self.api
+        rec = (lambda j: ev[j].record(stream)) if ev is not None else (lambda j: None)
+        rec(0)
+        a.cc_conv3d_causal(self.conv_x, self.conv_wp, self.conv_b, self.conv_y, stream=stream)
+        rec(1)
+        a.cc_attn_scores(self.q, self.k, self.s, stream=stream)
+        rec(2)
+        a.cc_attn_softmax(self.s, self.p, self.at.hw, self.scale, stream=stream)
+        rec(3)
+        a.cc_attn_pv(self.p, self.v, self.o, self.at.hw, stream=stream)
+        rec(4)
+        a.cc_resample_phase_conv(self.res_x, self.res_pw, self.phases, stream=stream)
+        rec(5)
+        a.cc_resample_interleave(self.phases, self.res_b, self.res_skip, self.res_out, stream=stream)
+        rec(6)
+        a.cc_head_temporal(self.head_x, self.head_wp, self.g, stream=stream)
+        rec(7)
+        a.cc_head_stencil(self.g, self.head_b, self.head_out, stream=stream)
+        rec(8)
+
+    # ---- end to end through host buffers -------------------------------
+    def host_buffers(self):
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        self.h_in = {"conv_x": pin(self.conv_x), "q": pin(self.q), "k": pin(self.k), "v": pin(self.v),
+                     "res_x": pin(self.res_x), "res_skip": pin(self.res_skip), "head_x": pin(self.head_x)}
+        self.h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                      for n, t in (("conv_y", self.conv_y), ("o", self.o), ("res_out", self.res_out),
+                                   ("head_out", self.head_out))}
+        dev_in = {"conv_x": self.conv_x, "q": self.q, "k": self.k, "v": self.v, "res_x": self.res_x,
+                  "res_skip": self.res_skip, "head_x": self.head_x}
+        self.d_in = dev_in
+        h2d = sum(t.numel() * t.element_size() for t in self.h_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in self.h_out.values())
+        return h2d, d2h
+
+    def step_e2e(self, stream):
+        with torch.cuda.stream(stream):
+            for n, t in self.h_in.items():
+                self.d_in[n].copy_(t, non_blocking=True)
+            self.step(stream)
+            self.h_out["conv_y"].copy_(self.conv_y, non_blocking=True)
+            self.h_out["o"].copy_(self.o, non_blocking=True)
+            self.h_out["res_out"].copy_(self.res_out, non_blocking=True)
+            self.h_out["head_out"].copy_(self.head_out, non_blocking=True)
+
+
+# -------------------------------------------------------------- CPU oracle --
+
+def oracle_sample_step(cpu, budget_s: float, rng):
+    """Times the fp64 oracle on a bounded sample of each stage's outputs and
+    extrapolates by output count to ms per chunk. Returns (ms_per_chunk,
+    seconds spent, description)."""
+    import oracle
+
+    total_ms = 0.0
+    spent = 0.0
+    desc = []
+    per_stage = budget_s / 4.0
+
+    def timed(fn, npts, total):
+        t0 = time.perf_counter()
+        fn(npts)
+        dt = time.perf_counter() - t0
+        return dt, dt * total / npts
+
+    stages = []
+    cv = cc_inputs.CONFIGS["mid_conv"]
+    stages.append(("conv", cv.n * cv.d * cv.h * cv.w,
+                   lambda P: oracle.causal_conv3d_at(cpu["conv_x"], cpu["conv_w"], cpu["conv_b"],
+                                                     _pts(rng, P, cv.n, cv.d, cv.h, cv.w))))
+    at = cc_inputs.CONFIGS["attention"]
+    stages.append(("attention", at.d * at.hw,
+                   lambda P: oracle.attn_frame_rows(cpu["q"], cpu["k"], cpu["v"],
+                                                    np.stack([rng.integers(0, at.d, P), rng.integers(0, at.hw, P)], 1))))
+    rs = cc_inputs.CONFIGS["resampler"]
+    stages.append(("resampler", rs.n * rs.d * 4 * rs.h * rs.w,
+                   lambda P: oracle.resample_up2_at(cpu["res_x"], cpu["res_w"], cpu["res_b"], cpu["res_skip"],
+                                                    _pts(rng, P, rs.n, rs.d, 2 * rs.h, 2 * rs.w))))
+    hd = cc_inputs.CONFIGS["head"]
+    hf = cpu["head_x"].shape[1]  # frames held on the host (the first ones)
+    stages.append(("head", hd.n * hd.d * hd.h * hd.w,
+                   lambda P: oracle.head_out_at(cpu["head_x"], cpu["head_w"], cpu["head_b"],
+                                                _pts(rng, P, hd.n, hf, hd.h, hd.w))))
+    for name, total, fn in stages:
+        npts = 8
+        dt, ms = timed(fn, npts, total)
+        spent += dt
+        if dt < per_stage / 4:
+            npts = int(min(4096, max(8, npts * per_stage / max(dt, 1e-4))))
+            dt, ms = timed(fn, npts, total)
+            spent += dt
+        total_ms += ms * 1e3
+        desc.append(f"{name}: {npts} of {total} outputs")
+    return total_ms, spent, "; ".join(desc) + " (extrapolated by output count)"
+
+
+def _pts(rng, p, n, d, h, w):
+    return np.stack([rng.integers(0, n, p), rng.integers(0, d, p), rng.integers(0, h, p), rng.integers(0, w, p)], 1)
+
+
+def host_inputs(device, head_frames=3):
+    """The oracle's inputs on the host (the head keeps its first frames only:
+    sampled outputs there need frames t-2..t, all held)."""
+    f = lambda t: t.float().cpu().numpy()
+    out = {}
+    i = cc_inputs.make_config_inputs("mid_conv", device)
+    out.update(conv_x=f(i["x"]), conv_w=f(i["w"]), conv_b=f(i["b"]))
+    i = cc_inputs.make_config_inputs("attention", device)
+    out.update(q=f(i["q"]), k=f(i["k"]), v=f(i["v"]))
+    i = cc_inputs.make_config_inputs("resampler", device)
+    out.update(res_x=f(i["x"]), res_w=f(i["w"]), res_b=f(i["b"]), res_skip=f(i["skip"]))
+    i = cc_inputs.make_config_inputs("head", device)
+    out.update(head_x=f(i["x"][:, :head_frames]), head_w=f(i["w"]), head_b=f(i["b"]))
+    return out
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# -------------------------------------------------------------------- main --
+
+def config_dict(n_gpus):
+    return {"workload": WORKLOAD, "chunks_per_step": n_gpus, "global_batch": n_gpus, "seq_len": 4,
+            "parallelism": f"replicas{n_gpus}" if n_gpus > 1 else "single",
+            "l2": "per-step working set ~4.3 GB > 126 MB L2: inputs larger than L2, no explicit flush"}
+
+
+def max_over_ranks(value: float, device) -> float:
+    """The maximum of `value` over all ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, local = dist_setup()
+    if rank != 0:
+        return 0
+    device = "cuda:0" if torch.cuda.is_available() else "cpu"
+    cpu = host_inputs(device)
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle_sample_step(cpu, args.ref_step_s, rng)
+    vals, spent, desc = [], 0.0, ""
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, s, desc = oracle_sample_step(cpu, args.ref_step_s, rng)
+        vals.append(v)
+        spent += s
+    wall = time.perf_counter() - t0
+    value = float(np.mean(vals)) / max(args.gpus, 1)
+    cores = cpu_threads()
+    line = {"metric": METRIC, "value": value, "unit": "ms", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(args.gpus), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle",
+                             "sample": f"per step: {desc}; fp64 numpy oracle on {cores} host threads"},
+            "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=16.0)
+    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    device = torch.device(f"cuda:{local}")
+
+    from causal_convolution_gb300 import _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        from causal_convolution_gb300 import build
+        build.build()
+
+    wl = Workload(device)
+    stream = torch.cuda.Stream(device)
+    for _ in range(args.warmup):
+        wl.step(stream)
+    torch.cuda.synchronize(device)
+    wl.api.cc_check_device()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    clocks.start()
+    time.sleep(0.25)
+    t_start.record(stream)
+    for k in range(args.steps):
+        wl.step(stream, evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    clocks.stop()
+    if ws > 1:
+        torch.distributed.barrier()
+    wl.api.cc_check_device()
+    elapsed = t_start.elapsed_time(t_end)
+    per_kernel = {name: float(np.mean([evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)]))
+                  for j, name in enumerate(KERNELS)}
+    ms_step = max_over_ranks(elapsed / args.steps, device)
+
+    # end to end: host buffers, copies inside the timed region
+    h2d, d2h = wl.host_buffers()
+    wl.step_e2e(stream)
+    torch.cuda.synchronize(device)
+    if ws > 1:
+        torch.distributed.barrier()
+    e0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        wl.step_e2e(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks((time.perf_counter() - e0) * 1e3 / args.e2e_steps, device)
+    wl.api.cc_check_device()
+
+    peaks = load_peaks()
+    work = algorithmic_work()
+    roofs = {}
+    for name in KERNELS:
+        bound, amount, unit = work[name]
+        sec = per_kernel[name] * 1e-3
+        if bound == "tensor":
+            ach = amount / sec / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            roofs[name] = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                           "ms": per_kernel[name], "work": amount}
+        else:
+            ach = amount / sec / 1e9
+            peak = peaks["hbm_gbs"]
+            roofs[name] = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                           "ms": per_kernel[name], "work": amount}
+    dominant = max(KERNELS, key=lambda n: per_kernel[n])
+    dr = roofs[dominant]
+    roofline = {"bound": dr["bound"], "achieved": round(dr["achieved"], 2), "peak": dr["peak"], "unit": dr["unit"],
+                "frac": round(dr["frac"], 4), "traffic": None, "kernel": dominant,
+                "peak_source": f"{peaks['source']} ({'sustained bf16' if dr['bound'] == 'tensor' else 'copy'})"}
+
+    line = {
+        "metric": METRIC, "value": round(ms_step / ws, 4), "unit": "ms", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal inputs, fan-in-scaled weights)",
+        "config": config_dict(ws),
+        "conv_tflops": round(roofs["conv3d_causal"]["achieved"], 2),
+        "conv_frac_of_bf16_peak": round(roofs["conv3d_causal"]["frac"], 4),
+        "resampler_interleave_gbs": round(roofs["resample_interleave"]["achieved"], 1),
+        "resampler_interleave_frac_of_hbm": round(roofs["resample_interleave"]["frac"], 4),
+        "head_stencil_gbs": round(roofs["head_stencil"]["achieved"], 1),
+        "stage_ms": {"conv": per_kernel["conv3d_causal"],
+                     "attention": per_kernel["attn_scores"] + per_kernel["attn_softmax"] + per_kernel["attn_pv"],
+                     "resampler": per_kernel["resample_phase_conv"] + per_kernel["resample_interleave"],
+                     "head": per_kernel["head_temporal"] + per_kernel["head_stencil"]},
+        "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()} for n, r in roofs.items()},
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_ms / ws, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": len(KERNELS) * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = host_inputs(device)
+        v, spent, desc = oracle_sample_step(cpu, args.cpu_budget_s, np.random.default_rng(0))
+        line["cpu_baseline"] = {"value": round(v, 1), "unit": "ms", "cores": cpu_threads(), "kind": "oracle",
+                                "sample": f"{desc}; {spent:.1f} s of fp64 numpy oracle work"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

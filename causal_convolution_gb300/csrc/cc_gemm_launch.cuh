@@ -1,0 +1,28 @@
+// Host-side launch of the tcgen05 implicit GEMM (one persistent CTA per SM).
+#pragma once
+
+#include <algorithm>
+
+#include "cc_gemm.cuh"
+#include "cc_host.h"
+
+namespace cc {
+
+template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS>
+cc_status launch_tc_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs& args, const DeviceInfo& di,
+                         cudaStream_t stream, const char* what) {
+  using S = GemmShape<BN>;
+  if (args.num_tiles <= 0) return CC_OK;
+  auto kern = tc_gemm_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: shared-memory attribute: %s", what, cudaGetErrorString(e));
+  args.err = di.err_word;
+  args.timeout_ns = kWaitLimitNs;
+  const int grid = std::min(args.num_tiles, di.sm_count);
+  kern<<<grid, kGemmThreads, S::kSmemBytes, stream>>>(ta, tb, args);
+  return launch_status(what);
+}
+
+inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+}  // namespace cc

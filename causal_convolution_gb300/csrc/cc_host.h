@@ -1,0 +1,45 @@
+// Host-side helpers shared by the translation units of the library: the
+// thread-local error message, argument checks, tensor-map encoding through
+// the driver entry points, and per-device facts (SM count, error word).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstddef>
+#include <cstdint>
+
+#include "cc.h"
+
+namespace cc {
+
+// Records a printf-style message as the calling thread's last error and
+// returns `st` so call sites can `return fail(CC_ERR_INVALID, "...")`.
+cc_status fail(cc_status st, const char* fmt, ...);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-device facts, cached on first use.
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  unsigned int* err_word;  // device address of the library's error word
+};
+cc_status device_info(DeviceInfo* out);
+
+// Kernel launch wrapper: maps cudaGetLastError into a status.
+cc_status launch_status(const char* what);
+
+// Tensor maps (bf16 elements unless stated).
+cc_status encode_im2col_5d(CUtensorMap* map, const void* base, int n, int d, int h, int w, int c, int lo_w, int lo_h,
+                           int lo_d, int up_w, int up_h, int up_d, int pixels, int channels);
+cc_status encode_tiled_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                          uint32_t box_inner, uint32_t box_outer);
+cc_status encode_tiled_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                          uint64_t stride2, uint32_t box0, uint32_t box1);
+
+// Upper bound on one mbarrier wait inside the library's kernels.
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+
+}  // namespace cc

@@ -1,0 +1,194 @@
+/*
+ * cc.h -- C ABI of the GB300 causal-convolution library (libcc.so).
+ *
+ * The bf16 causal 3-D convolution stack of the Wan2.2 (TI2V-5B style) video
+ * VAE decoder: the causal 3x3x3 convolution, the nearest-x2 spatial
+ * resampler (four pre-summed phase convolutions + one interleave pass), the
+ * mid-block per-frame single-head attention and the output head (conv_out to
+ * 12 channels, bias, clamp). All compute runs in the library's own sm_103a
+ * kernels; nothing here falls back to the CPU.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are DEVICE pointers owned by the caller. The library allocates
+ *    no device memory: intermediates live in a caller-provided workspace
+ *    whose size the matching *_workspace_bytes() function returns.
+ *  - bf16 tensors are passed as raw 16-bit patterns (cc_bf16 = uint16_t).
+ *  - Activations are channels-last: [N, D, H, W, C] contiguous, C fastest.
+ *    Convolution weights keep the PyTorch Conv3d order [C_out, C_in, 3, 3, 3]
+ *    until a *_prepare() call repacks them.
+ *  - Every pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *    asynchronous on it; the caller keeps every buffer alive until the work
+ *    on the stream is done.
+ *  - Arguments are checked on the host before any launch. A rejected call
+ *    launches nothing and returns CC_ERR_INVALID or CC_ERR_UNSUPPORTED;
+ *    cc_last_error() then describes the reason. No C++ exception crosses
+ *    the ABI.
+ *  - Kernels never trap. A pipeline wait that runs past its time limit makes
+ *    the kernel wind down and set a device error word, which
+ *    cc_check_device() reports as CC_ERR_TIMEOUT.
+ *  - `hist` selects what precedes frame 0 in time: 0 = two zero frames (the
+ *    causal zero padding), x then holds D frames; 2 = x holds two history
+ *    frames in front of its D frames (D + 2 frames in total), so a chunked
+ *    decode can carry the previous chunk's last two frames.
+ *
+ * Sources for the definitions (pages of the reference material):
+ *  [ATTN] FastVideo wan22_vae_decode solution/attn.cu -- header comment and
+ *         attn_forward: per-frame softmax(q k^T / sqrt(C)) v, no mask.
+ *  [RES]  FastVideo wan22_vae_decode solution/resample.h -- header comment
+ *         (four-phase decomposition, interleave pass) and the comment on
+ *         resample_upsample (history frames, phase order 2*row_parity +
+ *         col_parity).
+ *  [HEAD] FastVideo wan22_vae_decode solution/head.cu -- header comment
+ *         (conv_out folded into a 3x1x1 conv with 9x12 output channels, then
+ *         a 3x3 stencil, bias and clamp) and head_stencil_kernel.
+ *  [TASK] the stack's definition: causal 3x3x3 conv with two history frames,
+ *         zeros before frame 0, spatial zero padding 1, fp32 accumulation.
+ */
+#ifndef CC_H_
+#define CC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t cc_bf16;
+
+typedef enum cc_status {
+  CC_OK = 0,
+  CC_ERR_INVALID = 1,     /* null/misaligned pointer, bad size or shape     */
+  CC_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels cover  */
+  CC_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed    */
+  CC_ERR_TIMEOUT = 4,     /* a kernel wait ran past its limit (see above)  */
+  CC_ERR_DEVICE = 5       /* a kernel-side index check failed              */
+} cc_status;
+
+/* Message describing the calling thread's most recent failure ("" if none). */
+const char* cc_last_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int cc_version(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word. Returns CC_OK, CC_ERR_TIMEOUT, CC_ERR_DEVICE or CC_ERR_CUDA. */
+cc_status cc_check_device(void* stream);
+
+/* ------------------------------------------------ causal 3x3x3 conv [TASK] */
+
+/* Repacks w [C_out, C_in, 3, 3, 3] into wp [27][C_out][C_in] (tap-major,
+ * tap = kt*9 + kh*3 + kw, each row K-major), the B operand of the implicit
+ * GEMM. wp holds 27*C_out*C_in elements. */
+cc_status cc_conv3d_prepare(const cc_bf16* w, cc_bf16* wp, int cout, int cin, void* stream);
+
+/* y[n,t,h,w,co] = bias[co] + sum_{ci,kt,kh,kw} W[co,ci,kt,kh,kw]
+ *                          * x~[n, t+kt-2, h+kh-1, w+kw-1, ci]
+ * with x~ zero outside the plane and before frame 0 as `hist` says; fp32
+ * accumulation, one rounding to bf16. x: [N, D+hist, H, W, C_in]; wp from
+ * cc_conv3d_prepare; bias [C_out] or NULL; y: [N, D, H, W, C_out].
+ * Needs C_in % 64 == 0 and C_out % 16 == 0. */
+cc_status cc_conv3d_causal(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* y, int n, int d,
+                           int h, int w, int cin, int cout, int hist, void* stream);
+
+/* ------------------------------------------------ spatial resampler [RES] */
+
+/* Pre-sums the taps that nearest-x2 makes coincide. For output parity
+ * (p, q) and phase tap (kt, a, b), rows {0} | {1,2} (p=0, a=0|1) or {0,1} | {2}
+ * (p=1) and the same for columns are summed in fp32 and rounded once:
+ * pw[(2p+q)][(kt*2+a)*2+b][co][ci]; 48*C_out*C_in elements. */
+cc_status cc_resample_prepare(const cc_bf16* w, cc_bf16* pw, int cout, int cin, void* stream);
+
+/* Bytes of workspace cc_resample_up2 needs: the four phase tensors. */
+size_t cc_resample_workspace_bytes(int n, int d, int hl, int wl, int cout);
+
+/* The four phase convolutions at low resolution (no bias):
+ * phases[2p+q][n,t,i,j,co] = sum_{ci,kt,a,b} pw[2p+q][(kt*2+a)*2+b][co][ci]
+ *                            * x~[n, t+kt-2, i+p-1+a, j+q-1+b, ci].
+ * x: [N, D+hist, HL, WL, C_in]; phases: 4 x [N, D, HL, WL, C_out] back to back.
+ * Needs C_in % 64 == 0 and C_out % 16 == 0. */
+cc_status cc_resample_phase_conv(const cc_bf16* x, const cc_bf16* pw, cc_bf16* phases, int n, int d, int hl,
+                                 int wl, int cin, int cout, int hist, void* stream);
+
+/* The interleave pass: out[n,t,2i+p,2j+q,c] = phases[2p+q][n,t,i,j,c] + bias[c]
+ * + skip[n,t,i,j,c], summed in fp32 and rounded once. skip: [N, D, HL, WL, C];
+ * out: [N, D, 2HL, 2WL, C]. Needs C % 8 == 0. */
+cc_status cc_resample_interleave(const cc_bf16* phases, const cc_bf16* bias, const cc_bf16* skip, cc_bf16* out,
+                                 int n, int d, int hl, int wl, int c, void* stream);
+
+/* Whole resampler: nearest x2 in space, causal 3x3x3 conv, bias, plus the
+ * nearest-duplicated shortcut `skip` (same channel count as the output).
+ * out: [N, D, 2HL, 2WL, C_out]. ws: at least cc_resample_workspace_bytes(). */
+cc_status cc_resample_up2(const cc_bf16* x, const cc_bf16* pw, const cc_bf16* bias, const cc_bf16* skip,
+                          cc_bf16* out, int n, int d, int hl, int wl, int cin, int cout, int hist, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------ per-frame attention [ATTN] */
+
+/* Row stride (elements) used for S (fp32) and P (bf16) inside the workspace. */
+int64_t cc_attn_ld(int hw);
+
+/* Bytes of workspace cc_attn_frame needs: S fp32 and P bf16, T*HW rows each. */
+size_t cc_attn_workspace_bytes(int t, int hw);
+
+/* S[f,i,j] = sum_c q[f,i,c] k[f,j,c] in fp32 (unscaled). q, k: T frames of HW
+ * rows with row strides ld_q, ld_k elements (frame stride HW*ld); s: row
+ * stride ld_s floats. Needs C % 64 == 0, ld_q and ld_k % 8 == 0,
+ * ld_s % 4 == 0, ld_s >= HW. */
+cc_status cc_attn_scores(const cc_bf16* q, const cc_bf16* k, float* s, int t, int hw, int c, int64_t ld_q,
+                         int64_t ld_k, int64_t ld_s, void* stream);
+
+/* P[f,i,j] = bf16( exp(scale*S[f,i,j] - m_i) / sum_j exp(scale*S[f,i,j] - m_i) ),
+ * m_i = max_j scale*S[f,i,j]; columns HW..ld_p-1 of P are written as zero.
+ * Needs ld_s % 4 == 0, ld_p % 8 == 0, ld_p >= HW, scale > 0. */
+cc_status cc_attn_softmax(const float* s, cc_bf16* p, int t, int hw, int64_t ld_s, int64_t ld_p, float scale,
+                          void* stream);
+
+/* O[f,i,c] = sum_j P[f,i,j] v[f,j,c], fp32 accumulation, bf16 out. v is read
+ * as stored ([j][c], no transpose). Needs C % 64 == 0, ld_p, ld_v, ld_o % 8 == 0. */
+cc_status cc_attn_pv(const cc_bf16* p, const cc_bf16* v, cc_bf16* o, int t, int hw, int c, int64_t ld_p,
+                     int64_t ld_v, int64_t ld_o, void* stream);
+
+/* Whole attention: O = softmax(q k^T * scale) v per frame, no mask (scale is
+ * 1/sqrt(C) in the decoder). Packed qkv [T, HW, 3C] works with
+ * ld_q = ld_k = ld_v = 3C and k = q + C, v = q + 2C.
+ * ws: at least cc_attn_workspace_bytes(). */
+cc_status cc_attn_frame(const cc_bf16* q, const cc_bf16* k, const cc_bf16* v, cc_bf16* o, int t, int hw, int c,
+                        int64_t ld_q, int64_t ld_k, int64_t ld_v, int64_t ld_o, float scale, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------ output head [HEAD] */
+
+#define CC_HEAD_COUT 12
+#define CC_HEAD_G_CH 112 /* 9 spatial taps x 12 channels, padded to 112 */
+
+/* Repacks conv_out's w [12, C_in, 3, 3, 3] into wp [3][112][C_in]:
+ * wp[kt][(i*3+j)*12 + c][ci] = w[c][ci][kt][i][j]; rows 108..111 are zero. */
+cc_status cc_head_prepare(const cc_bf16* w, cc_bf16* wp, int cin, void* stream);
+
+/* Bytes of workspace cc_head_out needs: g, [N, D, H, W, 112] bf16. */
+size_t cc_head_workspace_bytes(int n, int d, int h, int w);
+
+/* Stage A, the temporal-only part of conv_out:
+ * g[n,t,h,w,r] = sum_{ci,kt} wp[kt][r][ci] x~[n, t+kt-2, h, w, ci] (fp32 acc,
+ * bf16 out). x: [N, D+hist, H, W, C_in], C_in % 64 == 0. */
+cc_status cc_head_temporal(const cc_bf16* x, const cc_bf16* wp, cc_bf16* g, int n, int d, int h, int w, int cin,
+                           int hist, void* stream);
+
+/* Stage B: out[n,t,h,w,c] = clamp(bias[c] + sum_{i,j} g[n,t,h+i-1,w+j-1,(i*3+j)*12+c],
+ * -1, 1), zero outside the plane, fp32 sum, one bf16 rounding.
+ * g: [N, D, H, W, 112]; out: [N, D, H, W, 12]. */
+cc_status cc_head_stencil(const cc_bf16* g, const cc_bf16* bias, cc_bf16* out, int n, int d, int h, int w,
+                          void* stream);
+
+/* Whole head: causal conv_out 3x3x3 C_in -> 12, bias, clamp to [-1, 1].
+ * out: [N, D, H, W, 12]; ws: at least cc_head_workspace_bytes(). */
+cc_status cc_head_out(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* out, int n, int d, int h,
+                      int w, int cin, int hist, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CC_H_ */

@@ -49,12 +49,16 @@ __all__ = [
     "resample_up2",
     "resample_up2_at",
     "resample_phase_kernels",
+    "resample_phase_conv",
+    "resample_interleave",
     "resample_up2_four_phase",
     "attn_probs",
     "attn_frame",
     "attn_frame_rows",
     "head_out",
     "head_out_at",
+    "head_stage_a",
+    "head_stage_b",
     "head_two_stage",
 ]
 
@@ -108,7 +112,7 @@ def causal_conv3d_at(x, w, b, points, history=None) -> np.ndarray:
     """The same convolution evaluated only at ``points`` (an int array [P,4]
     of (n, t, h, w)); returns [P, Cout]. Used where the full output is too
     large for the CPU."""
-    x = _f64(x) if x.dtype != np.float64 else x
+    x = np.asarray(x)  # gathered windows are widened to float64 below
     w = _f64(w)
     pts = np.asarray(points, dtype=np.int64).reshape(-1, 4)
     n, d, h, wd, cin = x.shape
@@ -116,7 +120,7 @@ def causal_conv3d_at(x, w, b, points, history=None) -> np.ndarray:
     out = np.zeros((len(pts), cout), dtype=np.float64)
     if b is not None:
         out += _f64(b)
-    hist = None if history is None else _f64(history)
+    hist = None if history is None else np.asarray(history)
     for kt in range(3):
         for kh in range(3):
             for kw in range(3):
@@ -150,14 +154,14 @@ def resample_up2(x, w, b, skip, history=None) -> np.ndarray:
 def resample_up2_at(x, w, b, skip, points, history=None) -> np.ndarray:
     """The direct resampler at high-resolution ``points`` [P,4] of
     (n, t, y, x); the up-sampled tensor is indexed, never materialised."""
-    x = _f64(x) if x.dtype != np.float64 else x
+    x = np.asarray(x)  # gathered windows are widened to float64 below
     w = _f64(w)
     pts = np.asarray(points, dtype=np.int64).reshape(-1, 4)
     n, d, hl, wl, cin = x.shape
     hh_max, ww_max = 2 * hl, 2 * wl
     cout = w.shape[0]
     out = np.zeros((len(pts), cout), dtype=np.float64) + _f64(b)
-    hist = None if history is None else _f64(history)
+    hist = None if history is None else np.asarray(history)
     for kt in range(3):
         for kh in range(3):
             for kw in range(3):
@@ -172,8 +176,8 @@ def resample_up2_at(x, w, b, skip, points, history=None) -> np.ndarray:
                     old = inside & (tt < 0)
                     win[old] = hist[pts[old, 0], tt[old] + 2, yy[old] // 2, xx[old] // 2, :]
                 out += win @ w[:, :, kt, kh, kw].T
-    s = skip if skip.dtype == np.float64 else _f64(skip)
-    out += s[pts[:, 0], pts[:, 1], pts[:, 2] // 2, pts[:, 3] // 2, :]
+    s = np.asarray(skip)
+    out += s[pts[:, 0], pts[:, 1], pts[:, 2] // 2, pts[:, 3] // 2, :].astype(np.float64)
     return out
 
 
@@ -203,29 +207,43 @@ def resample_phase_kernels(w) -> np.ndarray:
     return pk
 
 
-def resample_up2_four_phase(x, w, b, skip) -> np.ndarray:
-    """The resampler through the four-phase form, kept only to check the
-    decomposition against the direct form: each phase is a causal 3x2x2 conv
-    at low resolution, reading x~[t+kt-2, i+p-1+a, j+q-1+b]; the interleave
-    then writes out[t, 2i+p, 2j+q] = phase + bias + skip."""
+def resample_phase_conv(x, pk, history=None) -> np.ndarray:
+    """The four low-resolution phase convolutions (no bias): phase 2p+q at
+    (t, i, j) is sum_{ci,kt,a,b} pk[2p+q, co, ci, kt, a, b]
+    * x~[t+kt-2, i+p-1+a, j+q-1+b, ci]. Returns [4, N, D, HL, WL, Cout]."""
     x = _f64(x)
+    pk = _f64(pk)
     n, d, hl, wl, cin = x.shape
-    pk = resample_phase_kernels(w)
     cout = pk.shape[1]
-    xp = _pad_causal(x, None)  # index offset: frame +2, row +1, column +1
-    out = np.zeros((n, d, 2 * hl, 2 * wl, cout), dtype=np.float64)
-    s = _f64(skip)
+    xp = _pad_causal(x, history)  # index offset: frame +2, row +1, column +1
+    ph = np.zeros((4, n, d, hl, wl, cout), dtype=np.float64)
     for p in range(2):
         for q in range(2):
-            ph = np.zeros((n, d, hl, wl, cout), dtype=np.float64)
             for kt in range(3):
                 for a in range(2):
                     for bb in range(2):
                         r0 = p + a  # = (i + p - 1 + a) + 1 - i
                         c0 = q + bb
-                        ph += xp[:, kt:kt + d, r0:r0 + hl, c0:c0 + wl, :] @ pk[2 * p + q, :, :, kt, a, bb].T
-            out[:, :, p::2, q::2, :] = ph + _f64(b) + s
+                        ph[2 * p + q] += xp[:, kt:kt + d, r0:r0 + hl, c0:c0 + wl, :] @ pk[2 * p + q, :, :, kt, a, bb].T
+    return ph
+
+
+def resample_interleave(phases, b, skip) -> np.ndarray:
+    """out[n, t, 2i+p, 2j+q, c] = phases[2p+q][n, t, i, j, c] + b[c] + skip[n, t, i, j, c]."""
+    ph = _f64(phases)
+    _, n, d, hl, wl, c = ph.shape
+    out = np.zeros((n, d, 2 * hl, 2 * wl, c), dtype=np.float64)
+    for p in range(2):
+        for q in range(2):
+            out[:, :, p::2, q::2, :] = ph[2 * p + q] + _f64(b) + _f64(skip)
     return out
+
+
+def resample_up2_four_phase(x, w, b, skip, history=None) -> np.ndarray:
+    """The resampler through the four-phase form (pre-summed kernels, four
+    low-resolution convolutions, interleave with bias and shortcut), kept to
+    check the decomposition against the direct form."""
+    return resample_interleave(resample_phase_conv(x, resample_phase_kernels(w), history), b, skip)
 
 
 def attn_probs(q, k, scale=None) -> np.ndarray:
@@ -250,17 +268,17 @@ def attn_frame(q, k, v, scale=None) -> np.ndarray:
 
 def attn_frame_rows(q, k, v, rows, scale=None) -> np.ndarray:
     """Attention output for the query rows ``rows`` [P,2] of (frame, i)."""
-    q = _f64(q) if q.dtype != np.float64 else q
-    k = _f64(k) if k.dtype != np.float64 else k
-    v = _f64(v) if v.dtype != np.float64 else v
+    q, k, v = np.asarray(q), np.asarray(k), np.asarray(v)  # widened per frame below
     rows = np.asarray(rows, dtype=np.int64).reshape(-1, 2)
     if scale is None:
         scale = 1.0 / np.sqrt(q.shape[-1])
     out = np.zeros((len(rows), v.shape[-1]), dtype=np.float64)
-    for idx, (t, i) in enumerate(rows):
-        s = (k[t] @ q[t, i]) * scale
-        e = np.exp(s - s.max())
-        out[idx] = (e / e.sum()) @ v[t]
+    for t in np.unique(rows[:, 0]):
+        kt, vt = _f64(k[t]), _f64(v[t])
+        sel = np.nonzero(rows[:, 0] == t)[0]
+        s = (_f64(q[t, rows[sel, 1]]) @ kt.T) * scale
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        out[sel] = (e / e.sum(axis=1, keepdims=True)) @ vt
     return out
 
 
@@ -274,27 +292,43 @@ def head_out_at(x, w, b, points, history=None) -> np.ndarray:
     return np.clip(causal_conv3d_at(x, w, b, points, history), -1.0, 1.0)
 
 
-def head_two_stage(x, w, b) -> np.ndarray:
-    """The head regrouped as on the head.cu page, kept only to check that the
-    regrouping is the same sum: stage A is a temporal-only (3x1x1) conv whose
-    output channel (i*3+j)*12 + c holds spatial tap (i, j) of channel c; stage B
-    sums, at each position, tap (i, j) read from position (h+i-1, w+j-1)
-    (zero outside the plane), adds the bias and clamps."""
+def head_stage_a(x, w, history=None) -> np.ndarray:
+    """Stage A of the regrouped head: a temporal-only (3x1x1) conv whose output
+    channel (i*3+j)*Cout + c holds spatial tap (i, j) of channel c:
+    g[n,t,h,w,(i*3+j)*Cout+c] = sum_{ci,kt} w[c,ci,kt,i,j] x~[n, t+kt-2, h, w, ci]."""
     x = _f64(x)
     w = _f64(w)
     n, d, h, wd, cin = x.shape
     cout = w.shape[0]
     xp = np.zeros((n, d + 2, h, wd, cin), dtype=np.float64)
     xp[:, 2:] = x
+    if history is not None:
+        xp[:, :2] = _f64(history)
     g = np.zeros((n, d, h, wd, 9 * cout), dtype=np.float64)
     for i in range(3):
         for j in range(3):
             for kt in range(3):
                 g[..., (i * 3 + j) * cout:(i * 3 + j + 1) * cout] += xp[:, kt:kt + d] @ w[:, :, kt, i, j].T
+    return g
+
+
+def head_stage_b(g, b) -> np.ndarray:
+    """Stage B: out[n,t,h,w,c] = clamp(b[c] + sum_{i,j} g[n,t,h+i-1,w+j-1,(i*3+j)*Cout+c],
+    -1, 1), zero outside the plane."""
+    g = _f64(g)
+    b = _f64(b)
+    cout = b.shape[0]
+    n, d, h, wd, _ = g.shape
     gp = np.zeros((n, d, h + 2, wd + 2, 9 * cout), dtype=np.float64)
-    gp[:, :, 1:-1, 1:-1] = g
-    y = np.zeros((n, d, h, wd, cout), dtype=np.float64) + _f64(b)
+    gp[:, :, 1:-1, 1:-1] = g[..., :9 * cout]
+    y = np.zeros((n, d, h, wd, cout), dtype=np.float64) + b
     for i in range(3):
         for j in range(3):
             y += gp[:, :, i:i + h, j:j + wd, (i * 3 + j) * cout:(i * 3 + j + 1) * cout]
     return np.clip(y, -1.0, 1.0)
+
+
+def head_two_stage(x, w, b, history=None) -> np.ndarray:
+    """The head regrouped as on the head.cu page (stage A then stage B), kept
+    to check that the regrouping is the same sum as the direct conv."""
+    return head_stage_b(head_stage_a(x, w, history), b)

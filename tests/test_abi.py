@@ -1,0 +1,80 @@
+"""The C ABI without a GPU: libcc.so builds, loads, exports every function
+include/*.h declares, and rejects bad arguments on the host before touching
+the device. No compute call is made here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from causal_convolution_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include"))) if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from causal_convolution_gb300 import build
+        build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    names = set()
+    for path in HEADERS:
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(cc_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_headers_declare_the_boundary():
+    names = declared_functions()
+    for required in ("cc_conv3d_causal", "cc_resample_up2", "cc_attn_frame", "cc_head_out", "cc_check_device",
+                     "cc_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_python_binding_declares_every_symbol():
+    assert set(declared_functions()) == set(_lib.SIGNATURES)
+
+
+def test_version_and_workspace_arithmetic(lib):
+    assert lib.cc_version() >= 100
+    assert lib.cc_resample_workspace_bytes(1, 8, 88, 156, 512) == 4 * 8 * 88 * 156 * 512 * 2
+    assert lib.cc_head_workspace_bytes(1, 16, 352, 624) == 16 * 352 * 624 * 112 * 2
+    assert lib.cc_attn_ld(3432) == 3432
+    assert lib.cc_attn_ld(3433) == 3440
+    ld = 3432
+    assert lib.cc_attn_workspace_bytes(4, 3432) == 4 * 3432 * ld * 4 + 4 * 3432 * ld * 2
+    assert lib.cc_resample_workspace_bytes(0, 1, 1, 1, 1) == 0
+
+
+def test_host_validation_rejects_before_any_launch(lib):
+    # null pointers, misalignment and bad sizes come back as CC_ERR_INVALID /
+    # CC_ERR_UNSUPPORTED without a device (no CUDA call is reached)
+    buf = ctypes.create_string_buffer(1 << 12)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.cc_conv3d_causal(None, p, None, p, 1, 1, 1, 1, 64, 64, 0, None) == 1
+    assert b"null" in lib.cc_last_error()
+    assert lib.cc_conv3d_causal(p + 2, p, None, p, 1, 1, 1, 1, 64, 64, 0, None) == 1
+    assert b"aligned" in lib.cc_last_error()
+    assert lib.cc_conv3d_causal(p, p, None, p, 1, 1, 1, 1, 64, 64, 1, None) == 1  # hist must be 0 or 2
+    assert lib.cc_conv3d_causal(p, p, None, p, 1, 1, 1, 1, 48, 64, 0, None) == 2  # C_in % 64
+    assert b"multiple of 64" in lib.cc_last_error()
+    assert lib.cc_resample_interleave(p, p, p, p, 1, 1, 1, 1, 12, None) == 2  # C % 8
+    assert lib.cc_attn_softmax(p, p, 1, 16, 16, 16, ctypes.c_float(-1.0), None) == 1  # scale > 0
+    assert lib.cc_attn_frame(p, p, p, p, 1, 16, 64, 64, 64, 64, 64, ctypes.c_float(0.125), p, 16, None) == 1
+    assert b"workspace" in lib.cc_last_error()
+    assert lib.cc_head_out(p, p, p, p, 1, 1, 4, 4, 64, 0, p, 10, None) == 1
+    assert lib.cc_debug_wait_timeout(0, None) == 1
+    assert lib.cc_debug_im2col_tile(p, p, 1, 1, 1, 1, 64, -17, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == 1

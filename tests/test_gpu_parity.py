@@ -1,0 +1,391 @@
+"""GPU parity: every entry point of the C ABI against the fp64 oracle on the
+same seeded bf16 inputs.
+
+Small cases run the whole output through the oracle and are shaped to span
+several 128-row tiles with a ragged tail (and partial column tiles); the
+full-size configurations compare sampled outputs (tile boundaries, every
+corner and edge of every frame, and random positions) that the oracle
+computes one by one. The bar is the one stated for this stack: relative L2
+error <= 4e-3 and max |d| <= 2^-6 * max |ref| per output tensor; pure data
+movement (weight repacks) is compared bit for bit.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from causal_convolution_gb300 import api, inputs
+from gpu_util import assert_parity, edge_points, ensure_built, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BF16 = torch.bfloat16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    return ensure_built()
+
+
+def empty(*shape, dtype=BF16):
+    return torch.empty(shape, dtype=dtype, device=DEV)
+
+
+# ------------------------------------------------------------ im2col probe --
+
+def im2col_expected(x, lower, upper, start, offsets, c0):
+    """128 pixels walked W-fastest through the bounding box from `start`, each
+    read at pixel + offsets (zero outside the tensor)."""
+    n, d_in, h, w, _ = x.shape
+    box = [(lower[0], w - 1 + upper[0]), (lower[1], h - 1 + upper[1]), (lower[2], d_in - 1 + upper[2])]
+    pw, ph, pd, pn = start
+    out = np.zeros((128, 64), np.float32)
+    for p in range(128):
+        iw, ih, idd = pw + offsets[0], ph + offsets[1], pd + offsets[2]
+        if 0 <= pn < n and 0 <= idd < d_in and 0 <= ih < h and 0 <= iw < w:
+            out[p] = x[pn, idd, ih, iw, c0:c0 + 64]
+        pw += 1
+        if pw > box[0][1]:
+            pw = box[0][0]
+            ph += 1
+        if ph > box[1][1]:
+            ph = box[1][0]
+            pd += 1
+        if pd > box[2][1]:
+            pd = box[2][0]
+            pn += 1
+    return out
+
+
+@pytest.mark.parametrize("lower,upper,start,offsets,c0", [
+    ((-1, -1, -2), (-1, -1, -2), (-1, -1, -2, 0), (0, 0, 0), 0),
+    ((-1, -1, -2), (-1, -1, -2), (-1, -1, -2, 0), (2, 1, 2), 64),
+    ((-1, -1, -2), (-1, -1, -2), (0, 1, -1, 0), (1, 2, 1), 0),
+    ((-1, -1, 0), (-1, -1, -2), (-1, -1, 0, 0), (1, 1, 2), 64),
+])
+def test_im2col_tile_matches_definition(lower, upper, start, offsets, c0):
+    g = torch.Generator(device=DEV).manual_seed(5)
+    x = torch.randn((2, 3, 5, 7, 128), generator=g, device=DEV).to(BF16)
+    tile = empty(128, 64)
+    api.cc_debug_im2col_tile(x, tile, lower, upper, c0, start, offsets)
+    api.cc_check_device()
+    got = to_np(tile)
+    exp = im2col_expected(to_np(x), lower, upper, start, offsets, c0)
+    if not np.array_equal(got, exp):
+        alt = im2col_expected(to_np(x), lower[::-1], upper[::-1], start, offsets, c0)
+        raise AssertionError(f"im2col tile differs from the definition; matches reversed corner order: "
+                             f"{np.array_equal(got, alt)}; first bad pixel: {int(np.argmax(np.any(got != exp, 1)))}")
+
+
+# ------------------------------------------------------------------- conv --
+
+def run_conv(n, d, h, w, cin, cout, hist, seed=11, with_bias=True):
+    inp = inputs.conv_inputs(n, d, h, w, cin, cout, seed, device=DEV, history=bool(hist))
+    x = torch.cat([inp["hist"], inp["x"]], 1).contiguous() if hist else inp["x"]
+    wp = empty(27 * cout * cin)
+    api.cc_conv3d_prepare(inp["w"], wp)
+    y = empty(n, d, h, w, cout)
+    api.cc_conv3d_causal(x, wp, inp["b"] if with_bias else None, y, hist=hist)
+    api.cc_check_device()
+    return inp, wp, y
+
+
+def test_conv3d_prepare_is_a_pure_repack():
+    inp = inputs.conv_inputs(1, 1, 1, 1, 64, 48, seed=3, device=DEV)
+    wp = empty(27 * 48 * 64)
+    api.cc_conv3d_prepare(inp["w"], wp)
+    ref = inp["w"].permute(2, 3, 4, 0, 1).reshape(-1)
+    assert torch.equal(wp.view(torch.int16), ref.contiguous().view(torch.int16))
+
+
+@pytest.mark.parametrize("n,d,h,w,cin,cout,hist,bias", [
+    (1, 3, 5, 9, 64, 64, 0, True),       # 135 rows: two tiles, ragged tail
+    (2, 2, 6, 11, 128, 272, 0, True),    # two images; partial column tile (272 = 256 + 16)
+    (1, 3, 4, 7, 64, 32, 2, True),       # carried history frames
+    (1, 2, 3, 5, 192, 64, 0, False),     # no bias
+    (1, 1, 1, 1, 64, 16, 0, True),       # a single position
+])
+def test_conv3d_causal_small(n, d, h, w, cin, cout, hist, bias):
+    inp, _, y = run_conv(n, d, h, w, cin, cout, hist, with_bias=bias)
+    ref = oracle.causal_conv3d(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]) if bias else None,
+                               history=to_np(inp["hist"]) if hist else None)
+    assert_parity(to_np(y), ref, f"conv {n,d,h,w,cin,cout,hist}")
+
+
+def test_conv3d_mid_block_config_sampled():
+    c = inputs.CONFIGS["mid_conv"]
+    inp = inputs.make_config_inputs("mid_conv", device=DEV)
+    wp = empty(27 * c.cout * c.c)
+    api.cc_conv3d_prepare(inp["w"], wp)
+    y = empty(c.n, c.d, c.h, c.w, c.cout)
+    api.cc_conv3d_causal(inp["x"], wp, inp["b"], y)
+    api.cc_check_device()
+    pts = edge_points(c.n, c.d, c.h, c.w, 160, np.random.default_rng(1))
+    ref = oracle.causal_conv3d_at(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]), pts)
+    yy = to_np(y)[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]]
+    assert_parity(yy, ref, "mid_conv sampled")
+
+
+def test_conv3d_output_guard_bands_untouched():
+    n, d, h, w, cin, cout = 1, 2, 5, 6, 64, 48
+    inp = inputs.conv_inputs(n, d, h, w, cin, cout, 4, device=DEV)
+    wp = empty(27 * cout * cin)
+    api.cc_conv3d_prepare(inp["w"], wp)
+    size = n * d * h * w * cout
+    guard = 4096
+    buf = torch.full((size + 2 * guard,), 12345, dtype=torch.int16, device=DEV)
+    y = buf[guard:guard + size].view(BF16).view(n, d, h, w, cout)
+    api.cc_conv3d_causal(inp["x"], wp, inp["b"], y)
+    api.cc_check_device()
+    assert bool((buf[:guard] == 12345).all()) and bool((buf[guard + size:] == 12345).all())
+    ref = oracle.causal_conv3d(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]))
+    assert_parity(to_np(y), ref, "conv in guarded buffer")
+
+
+# -------------------------------------------------------------- resampler --
+
+def prepare_resample(w):
+    cout, cin = w.shape[:2]
+    pw = empty(48 * cout * cin)
+    api.cc_resample_prepare(w, pw)
+    return pw
+
+
+def test_resample_prepare_matches_oracle_phase_kernels():
+    inp = inputs.resample_inputs(1, 1, 1, 1, 64, seed=8, device=DEV)
+    pw = prepare_resample(inp["w"])
+    pk = oracle.resample_phase_kernels(to_np(inp["w"]))  # [4, co, ci, kt, a, b]
+    ref = pk.transpose(0, 3, 4, 5, 1, 2).reshape(-1)     # [phase][(kt*2+a)*2+b][co][ci]
+    got = to_np(pw).astype(np.float64)
+    # fp32 sums of at most four bf16 taps, rounded once: within bf16's half ulp
+    np.testing.assert_allclose(got, ref, rtol=2.0 ** -8, atol=1e-30)
+
+
+def run_resample(x, w, b, skip, hist=0):
+    n, dd, hl, wl, cin = x.shape
+    d = dd - hist
+    cout = w.shape[0]
+    pw = prepare_resample(w)
+    out = empty(n, d, 2 * hl, 2 * wl, cout)
+    ws = torch.empty(api.cc_resample_workspace_bytes(n, d, hl, wl, cout), dtype=torch.uint8, device=DEV)
+    api.cc_resample_up2(x, pw, b, skip, out, ws, hist=hist)
+    api.cc_check_device()
+    return pw, out, ws
+
+
+def test_resample_toy_config_full():
+    inp = inputs.make_config_inputs("toy_resampler", device=DEV)
+    _, out, _ = run_resample(inp["x"], inp["w"], inp["b"], inp["skip"])
+    ref = oracle.resample_up2(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]), to_np(inp["skip"]))
+    assert out.shape == (1, 2, 16, 24, 64)
+    assert_parity(to_np(out), ref, "toy resampler")
+
+
+@pytest.mark.parametrize("n,d,hl,wl,cin,cout,hist", [
+    (1, 3, 5, 7, 64, 128, 0),
+    (2, 2, 3, 4, 128, 64, 2),
+    (1, 2, 9, 13, 64, 272, 0),
+])
+def test_resample_small(n, d, hl, wl, cin, cout, hist):
+    g = torch.Generator(device=DEV).manual_seed(21)
+    x = torch.randn((n, d + hist, hl, wl, cin), generator=g, device=DEV).to(BF16)
+    w = (torch.randn((cout, cin, 3, 3, 3), generator=g, device=DEV) / (27 * cin) ** 0.5).to(BF16)
+    b = (torch.randn((cout,), generator=g, device=DEV) * 0.1).to(BF16)
+    s = torch.randn((n, d, hl, wl, cout), generator=g, device=DEV).to(BF16)
+    _, out, _ = run_resample(x, w, b, s, hist)
+    xn = to_np(x)
+    ref = oracle.resample_up2(xn[:, hist:], to_np(w), to_np(b), to_np(s), history=xn[:, :2] if hist else None)
+    assert_parity(to_np(out), ref, f"resampler {n,d,hl,wl,cin,cout,hist}")
+
+
+def test_resample_stages_separately():
+    n, d, hl, wl, cin, cout = 1, 2, 6, 10, 64, 64
+    inp = inputs.resample_inputs(n, d, hl, wl, cin, seed=9, device=DEV)
+    pw = prepare_resample(inp["w"])
+    phases = empty(4, n, d, hl, wl, cout)
+    api.cc_resample_phase_conv(inp["x"], pw, phases)
+    api.cc_check_device()
+    pk = to_np(pw).reshape(4, 3, 2, 2, cout, cin).transpose(0, 4, 5, 1, 2, 3)
+    ref = oracle.resample_phase_conv(to_np(inp["x"]), pk)
+    for ph in range(4):
+        assert_parity(to_np(phases[ph]), ref[ph], f"phase {ph}")
+    out = empty(n, d, 2 * hl, 2 * wl, cout)
+    api.cc_resample_interleave(phases, inp["b"], inp["skip"], out)
+    api.cc_check_device()
+    ref_out = oracle.resample_interleave(to_np(phases), to_np(inp["b"]), to_np(inp["skip"]))
+    assert_parity(to_np(out), ref_out, "interleave", rel_l2=3e-3)
+
+
+def test_resample_config_sampled():
+    c = inputs.CONFIGS["resampler"]
+    inp = inputs.make_config_inputs("resampler", device=DEV)
+    _, out, _ = run_resample(inp["x"], inp["w"], inp["b"], inp["skip"])
+    pts = edge_points(c.n, c.d, 2 * c.h, 2 * c.w, 160, np.random.default_rng(2))
+    ref = oracle.resample_up2_at(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]), to_np(inp["skip"]), pts)
+    got = to_np(out)[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]]
+    assert_parity(got, ref, "resampler sampled")
+
+
+# -------------------------------------------------------------- attention --
+
+def run_attn(q, k, v):
+    t, hw, c = q.shape
+    o = empty(t, hw, c)
+    ws = torch.empty(api.cc_attn_workspace_bytes(t, hw), dtype=torch.uint8, device=DEV)
+    api.cc_attn_frame(q, k, v, o, ws)
+    api.cc_check_device()
+    return o
+
+
+@pytest.mark.parametrize("t,hw,c", [(2, 200, 64), (1, 130, 128), (3, 64, 64), (1, 1, 64), (2, 333, 1024),
+                                    (1, 4200, 64)])
+def test_attn_small(t, hw, c):
+    inp = inputs.attn_inputs(t, hw, c, seed=31, device=DEV)
+    o = run_attn(inp["q"], inp["k"], inp["v"])
+    ref = oracle.attn_frame(to_np(inp["q"]), to_np(inp["k"]), to_np(inp["v"]))
+    assert_parity(to_np(o), ref, f"attention {t,hw,c}")
+
+
+def test_attn_packed_qkv_layout():
+    t, hw, c = 2, 150, 128
+    g = torch.Generator(device=DEV).manual_seed(4)
+    qkv = torch.randn((t, hw, 3 * c), generator=g, device=DEV).to(BF16)
+    q, k, v = qkv[..., :c], qkv[..., c:2 * c], qkv[..., 2 * c:]
+    o = run_attn(q, k, v)
+    ref = oracle.attn_frame(to_np(q), to_np(k), to_np(v))
+    assert_parity(to_np(o), ref, "packed qkv")
+
+
+def test_attn_stages_separately():
+    t, hw, c = 2, 260, 128
+    inp = inputs.attn_inputs(t, hw, c, seed=32, device=DEV)
+    ld = api.cc_attn_ld(hw)
+    s = empty(t, hw, ld, dtype=torch.float32)
+    api.cc_attn_scores(inp["q"], inp["k"], s)
+    p = empty(t, hw, ld)
+    api.cc_attn_softmax(s, p, hw, c ** -0.5)
+    o = empty(t, hw, c)
+    api.cc_attn_pv(p, inp["v"], o, hw)
+    api.cc_check_device()
+    qn, kn, vn = to_np(inp["q"]), to_np(inp["k"]), to_np(inp["v"])
+    s_ref = np.einsum("tic,tjc->tij", qn.astype(np.float64), kn.astype(np.float64))
+    assert_parity(to_np(s)[:, :, :hw], s_ref, "scores", rel_l2=1e-5, max_frac=1e-5)
+    pn = to_np(p)
+    assert_parity(pn[:, :, :hw], oracle.attn_probs(qn, kn), "probabilities")
+    assert np.all(pn[:, :, hw:] == 0)
+    # O from the GPU's own P: isolates the PV product
+    o_ref = np.einsum("tij,tjc->tic", pn[:, :, :hw].astype(np.float64), vn.astype(np.float64))
+    assert_parity(to_np(o), o_ref, "pv", rel_l2=2e-3)
+
+
+def test_attn_config_sampled():
+    c = inputs.CONFIGS["attention"]
+    inp = inputs.make_config_inputs("attention", device=DEV)
+    o = run_attn(inp["q"], inp["k"], inp["v"])
+    rng = np.random.default_rng(3)
+    rows = [(t, i) for t in range(c.d) for i in (0, 127, 128, c.hw - 1)]
+    rows += [(int(rng.integers(c.d)), int(rng.integers(c.hw))) for _ in range(48)]
+    rows = np.array(rows)
+    ref = oracle.attn_frame_rows(to_np(inp["q"]), to_np(inp["k"]), to_np(inp["v"]), rows)
+    assert_parity(to_np(o)[rows[:, 0], rows[:, 1]], ref, "attention sampled")
+
+
+# ------------------------------------------------------------------- head --
+
+def run_head(x, w, b, hist=0):
+    n, dd, h, ww, cin = x.shape
+    d = dd - hist
+    wp = empty(3 * api.HEAD_G_CH * cin)
+    api.cc_head_prepare(w, wp)
+    out = empty(n, d, h, ww, api.HEAD_COUT)
+    ws = torch.empty(api.cc_head_workspace_bytes(n, d, h, ww), dtype=torch.uint8, device=DEV)
+    api.cc_head_out(x, wp, b, out, ws, hist=hist)
+    api.cc_check_device()
+    return wp, out, ws
+
+
+@pytest.mark.parametrize("n,d,h,w,cin,hist", [
+    (1, 3, 10, 14, 64, 0),
+    (1, 2, 8, 16, 128, 0),    # plane of 128: frame-interleaved tile order
+    (2, 2, 8, 16, 64, 0),
+    (1, 2, 5, 9, 64, 2),
+])
+def test_head_small(n, d, h, w, cin, hist):
+    g = torch.Generator(device=DEV).manual_seed(41)
+    x = (torch.randn((n, d + hist, h, w, cin), generator=g, device=DEV) * 2).to(BF16)
+    wt = (torch.randn((12, cin, 3, 3, 3), generator=g, device=DEV) / (27 * cin) ** 0.5).to(BF16)
+    b = (torch.randn((12,), generator=g, device=DEV) * 0.3).to(BF16)
+    _, out, _ = run_head(x, wt, b, hist)
+    xn = to_np(x)
+    ref = oracle.head_out(xn[:, hist:], to_np(wt), to_np(b), history=xn[:, :2] if hist else None)
+    assert_parity(to_np(out), ref, f"head {n,d,h,w,cin,hist}")
+    assert float(out.abs().max()) <= 1.0
+
+
+def test_head_stages_separately():
+    inp = inputs.head_inputs(1, 2, 6, 9, 64, seed=42, device=DEV)
+    wp = empty(3 * api.HEAD_G_CH * 64)
+    api.cc_head_prepare(inp["w"], wp)
+    gbuf = empty(1, 2, 6, 9, api.HEAD_G_CH)
+    api.cc_head_temporal(inp["x"], wp, gbuf)
+    api.cc_check_device()
+    g_ref = oracle.head_stage_a(to_np(inp["x"]), to_np(inp["w"]))
+    gn = to_np(gbuf)
+    assert_parity(gn[..., :108], g_ref, "head stage A")
+    assert np.all(gn[..., 108:] == 0)
+    out = empty(1, 2, 6, 9, 12)
+    api.cc_head_stencil(gbuf, inp["b"], out)
+    api.cc_check_device()
+    assert_parity(to_np(out), oracle.head_stage_b(gn, to_np(inp["b"])), "head stage B", rel_l2=3e-3)
+
+
+def test_head_prepare_is_a_pure_repack():
+    inp = inputs.head_inputs(1, 1, 1, 1, 64, seed=43, device=DEV)
+    wp = empty(3 * api.HEAD_G_CH * 64)
+    api.cc_head_prepare(inp["w"], wp)
+    w = inp["w"]  # [12, cin, 3, 3, 3]
+    ref = torch.zeros((3, api.HEAD_G_CH, 64), dtype=BF16, device=DEV)
+    ref[:, :108] = w.permute(2, 3, 4, 0, 1).reshape(3, 108, 64)
+    assert torch.equal(wp.view(3, api.HEAD_G_CH, 64).view(torch.int16), ref.view(torch.int16))
+
+
+def test_head_config_sampled():
+    c = inputs.CONFIGS["head"]
+    inp = inputs.make_config_inputs("head", device=DEV)
+    _, out, _ = run_head(inp["x"], inp["w"], inp["b"])
+    pts = edge_points(c.n, c.d, c.h, c.w, 400, np.random.default_rng(4))
+    ref = oracle.head_out_at(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]), pts)
+    got = to_np(out)[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]]
+    assert_parity(got, ref, "head sampled")
+
+
+# --------------------------------------------------------- failure paths --
+
+def test_unsupported_and_invalid_requests_raise():
+    x = empty(1, 1, 2, 2, 96)
+    wp = empty(27 * 16 * 96)
+    y = empty(1, 1, 2, 2, 16)
+    with pytest.raises(api.CCError) as e:
+        api.cc_conv3d_causal(x, wp, None, y)
+    assert e.value.status == 2
+    inp = inputs.resample_inputs(1, 1, 2, 2, 64, seed=1, device=DEV)
+    pw = prepare_resample(inp["w"])
+    out = empty(1, 1, 4, 4, 64)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(api.CCError) as e:
+        api.cc_resample_up2(inp["x"], pw, inp["b"], inp["skip"], out, ws)
+    assert e.value.status == 1
+    api.cc_check_device()
+
+
+def test_kernel_wait_timeout_is_reported_and_cleared():
+    api.cc_debug_wait_timeout(2_000_000)
+    with pytest.raises(api.CCError) as e:
+        api.cc_check_device()
+    assert e.value.status == 4
+    api.cc_check_device()  # the word was cleared; the context is still usable
+    inp, _, y = run_conv(1, 1, 2, 3, 64, 16, 0)
+    ref = oracle.causal_conv3d(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]))
+    assert_parity(to_np(y), ref, "conv after a timeout")

@@ -306,3 +306,27 @@ def test_head_sampled_matches_full():
     w, b = rnd(12, 8, 3, 3, 3) * 0.1, rnd(12) * 0.1
     pts = np.array(list(itertools.product(range(1), range(3), range(4), range(5))))
     np.testing.assert_allclose(oracle.head_out_at(x, w, b, pts), oracle.head_out(x, w, b)[0].reshape(-1, 12), atol=1e-12)
+
+
+def test_resample_four_phase_matches_direct_with_history():
+    x, s, hist = rnd(1, 2, 3, 4, 6), rnd(1, 2, 3, 4, 6), rnd(1, 2, 3, 4, 6)
+    w, b = rnd(5, 6, 3, 3, 3), rnd(5)
+    s = rnd(1, 2, 3, 4, 5)
+    np.testing.assert_allclose(oracle.resample_up2_four_phase(x, w, b, s, history=hist),
+                               oracle.resample_up2(x, w, b, s, history=hist), rtol=0, atol=1e-12)
+
+
+def test_head_two_stage_equals_direct_with_history():
+    x, hist = rnd(1, 2, 4, 5, 8), rnd(1, 2, 4, 5, 8)
+    w, b = rnd(12, 8, 3, 3, 3) * 0.05, rnd(12) * 0.1
+    np.testing.assert_allclose(oracle.head_two_stage(x, w, b, history=hist), oracle.head_out(x, w, b, history=hist),
+                               rtol=0, atol=1e-12)
+
+
+def test_interleave_places_each_phase_on_its_parity():
+    ph = rnd(4, 1, 2, 3, 4, 2)
+    b, s = rnd(2), rnd(1, 2, 3, 4, 2)
+    out = oracle.resample_interleave(ph, b, s)
+    # output row 2i+1, column 2j is phase 2*1+0 = 2
+    np.testing.assert_array_equal(out[0, 1, 2 * 2 + 1, 2 * 3, :], ph[2, 0, 1, 2, 3] + b + s[0, 1, 2, 3])
+    np.testing.assert_array_equal(out[0, 0, 0, 1, :], ph[1, 0, 0, 0, 0] + b + s[0, 0, 0, 0])
