@@ -194,8 +194,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) {
         // Let every copy already issued land before the CTA can exit: the
         // last armed phase of each stage is the only one that may be open.
+        // Copies land within microseconds; 200 ms per stage is ample.
         for (int s = 0; s < STAGES; ++s) {
-          (void)mbar_wait(smem_u32(&full[s]), (s < stage) ? phase : (phase ^ 1u), args.err, tlim);
+          (void)mbar_wait(smem_u32(&full[s]), (s < stage) ? phase : (phase ^ 1u), args.err, 200000000ull);
         }
       }
     }
