@@ -21,12 +21,14 @@ __all__ = [
     "cc_resample_up2",
     "cc_attn_ld", "cc_attn_workspace_bytes", "cc_attn_scores", "cc_attn_softmax", "cc_attn_pv", "cc_attn_frame",
     "cc_head_prepare", "cc_head_workspace_bytes", "cc_head_temporal", "cc_head_stencil", "cc_head_out",
+    "cc_head_out_noalloc", "HEAD_NOALLOC_SCRATCH_BYTES",
     "cc_debug_im2col_tile", "cc_debug_wait_timeout",
     "HEAD_COUT", "HEAD_G_CH",
 ]
 
 HEAD_COUT = 12
 HEAD_G_CH = 112
+HEAD_NOALLOC_SCRATCH_BYTES = 64 << 20  # CC_HEAD_NOALLOC_SCRATCH_BYTES
 
 STATUS = {0: "CC_OK", 1: "CC_ERR_INVALID", 2: "CC_ERR_UNSUPPORTED", 3: "CC_ERR_CUDA", 4: "CC_ERR_TIMEOUT",
           5: "CC_ERR_DEVICE"}
@@ -238,6 +240,19 @@ def cc_head_out(x, wp, bias, out, ws, hist: int = 0, stream=None) -> None:
     _check(_lib.load().cc_head_out(_ptr(x, name="x"), _ptr(wp, name="wp"), _ptr(bias, name="bias"),
                                    _ptr(out, name="out"), n, d, h, w, cin, hist, _ptr(ws, torch.uint8, "ws"),
                                    ws.numel(), _stream(stream)))
+
+
+def cc_head_out_noalloc(x, wp, bias, out, hist: int = 0, stream=None) -> None:
+    """cc_head_out without a workspace, for callers that cannot allocate device
+    memory: g lives in the library's fixed 64 MiB static scratch (at most
+    299,593 output positions per call; calls that overlap on the GPU race on
+    it, so keep them on one stream)."""
+    n, d, h, w, c = out.shape
+    cin = x.shape[-1]
+    if c != HEAD_COUT or tuple(x.shape) != (n, d + hist, h, w, cin) or bias.numel() != HEAD_COUT:
+        raise ValueError("head_out_noalloc: out must be [N,D,H,W,12] of x [N,D+hist,H,W,Cin]")
+    _check(_lib.load().cc_head_out_noalloc(_ptr(x, name="x"), _ptr(wp, name="wp"), _ptr(bias, name="bias"),
+                                           _ptr(out, name="out"), n, d, h, w, cin, hist, _stream(stream)))
 
 
 # ------------------------------------------------------------- self tests --

@@ -187,6 +187,31 @@ cc_status cc_head_stencil(const cc_bf16* g, const cc_bf16* bias, cc_bf16* out, i
 cc_status cc_head_out(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* out, int n, int d, int h,
                       int w, int cin, int hist, void* ws, size_t ws_bytes, void* stream);
 
+/* Size of the library's built-in scratch for cc_head_out_noalloc: 64 MiB,
+ * i.e. at most 64 MiB / (112 * 2 B) = 299,593 output positions per call. */
+#define CC_HEAD_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* The whole head, like cc_head_out, for callers that cannot allocate device
+ * memory and so cannot pass a workspace -- for example a plugin inside a host
+ * framework that owns every device allocation and exposes no allocator, or a
+ * latency-critical loop where cudaMalloc (which may synchronise the device) is
+ * not allowed. The paper has no counterpart to this entry point; it is an
+ * addition of this library. g lives in a fixed 64 MiB array in the library's static
+ * device memory, which every GPU that loads the library holds until the
+ * process exits; this function allocates nothing.
+ *  - The first call on a device looks up the array's device address (no
+ *    allocation) with that device current; make that first call before any
+ *    stream capture on the device.
+ *  - More than CC_HEAD_NOALLOC_SCRATCH_BYTES / 224 positions (N*D*H*W):
+ *    CC_ERR_INVALID with a message naming the limit; nothing is launched.
+ *  - All calls on a device share the array and leave their g in it; nothing
+ *    in it needs to start at zero (every element read is written first in the
+ *    same call). Calls whose GPU work overlaps (other streams or threads
+ *    without ordering) race on it: order them on one stream.
+ * Other arguments, layouts and errors as cc_head_out. */
+cc_status cc_head_out_noalloc(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* out, int n, int d,
+                              int h, int w, int cin, int hist, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,66 @@
+"""cc_head_out_noalloc: the output head for callers that cannot allocate device
+memory (for example a plugin whose host framework owns every device
+allocation and gives it no allocator, or a latency-critical loop where a
+cudaMalloc could synchronise the device), so they cannot pass the workspace
+cc_head_out needs. Its g intermediate lives in the library's fixed 64 MiB
+static scratch array instead.
+
+Checked through the C ABI against cc_head_out (the existing entry point) on
+the same inputs, on two calls in a row with different shapes, so a stale g
+left in the shared scratch by the first call would show in the second. This
+file sorts last so that a run stopping at its first failure has already run
+every other test; it also passes alone in a fresh process.
+"""
+
+import pytest
+import torch
+
+from causal_convolution_gb300 import api, inputs
+from gpu_util import assert_parity, ensure_built, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BF16 = torch.bfloat16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    return ensure_built()
+
+
+def both_entry_points(n, d, h, w, cin, seed):
+    inp = inputs.head_inputs(n, d, h, w, cin, seed=seed, device=DEV)
+    wp = torch.empty(3 * api.HEAD_G_CH * cin, dtype=BF16, device=DEV)
+    api.cc_head_prepare(inp["w"], wp)
+    ref = torch.empty((n, d, h, w, api.HEAD_COUT), dtype=BF16, device=DEV)
+    ws = torch.empty(api.cc_head_workspace_bytes(n, d, h, w), dtype=torch.uint8, device=DEV)
+    api.cc_head_out(inp["x"], wp, inp["b"], ref, ws)
+    got = torch.full((n, d, h, w, api.HEAD_COUT), float("nan"), dtype=BF16, device=DEV)
+    api.cc_head_out_noalloc(inp["x"], wp, inp["b"], got)
+    api.cc_check_device()
+    return got, ref
+
+
+def test_noalloc_head_matches_workspace_head_on_two_calls():
+    # first call: 109,824 positions, 24.6 MB of the 64 MiB scratch
+    got1, ref1 = both_entry_points(1, 2, 176, 312, 64, seed=51)
+    assert_parity(to_np(got1), to_np(ref1), "noalloc head, call 1")
+    # second call in a row: a different, smaller shape reuses the same scratch
+    got2, ref2 = both_entry_points(1, 2, 9, 13, 128, seed=52)
+    assert_parity(to_np(got2), to_np(ref2), "noalloc head, call 2")
+
+
+def test_noalloc_head_rejects_more_than_its_scratch_holds():
+    max_positions = api.HEAD_NOALLOC_SCRATCH_BYTES // (api.HEAD_G_CH * 2)
+    w = 512
+    h = max_positions // w + 1  # one frame just over the limit
+    x = torch.empty((1, 1, h, w, 64), dtype=BF16, device=DEV)
+    wp = torch.empty(3 * api.HEAD_G_CH * 64, dtype=BF16, device=DEV)
+    b = torch.zeros(12, dtype=BF16, device=DEV)
+    out = torch.empty((1, 1, h, w, 12), dtype=BF16, device=DEV)
+    with pytest.raises(api.CCError) as e:
+        api.cc_head_out_noalloc(x, wp, b, out)
+    assert e.value.status == 1
+    assert "scratch" in str(e.value)
+    api.cc_check_device()
