@@ -72,7 +72,7 @@ _GEMM_SRC = ["csrc/cc_gemm.cuh", "csrc/cc_ptx.cuh", "csrc/cc_gemm_launch.cuh", "
 KERNEL_SOURCES = {
     "conv3d_causal": _GEMM_SRC + ["csrc/conv.cu"],
     "resample_phase_conv": _GEMM_SRC + ["csrc/conv.cu"],
-    "head_temporal": _GEMM_SRC + ["csrc/conv.cu"],
+    "head_temporal": _GEMM_SRC + ["csrc/head.cu"],
     "attn_scores": _GEMM_SRC + ["csrc/attn.cu"],
     "attn_pv": _GEMM_SRC + ["csrc/attn.cu"],
     "attn_softmax": ["csrc/attn.cu"],

@@ -1,6 +1,6 @@
-// The convolutions: the causal 3x3x3 conv, the resampler's four phase convs
-// and the head's temporal stage -- one tcgen05 implicit GEMM fed by an im2col
-// TMA map over the channels-last input -- and their weight repacks.
+// The convolutions: the causal 3x3x3 conv and the resampler's four phase
+// convs -- one tcgen05 implicit GEMM fed by an im2col TMA map over the
+// channels-last input -- and their weight repacks.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -52,23 +52,6 @@ __global__ void resample_prepare_kernel(const __nv_bfloat16* __restrict__ w, __n
     for (int kh = r_lo; kh <= r_hi; ++kh)
       for (int kw = c_lo; kw <= c_hi; ++kw) s += bf(w, base + kh * 3 + kw);
     pw[i] = __float2bfloat16_rn(s);
-  }
-}
-
-// wp[kt][(i*3+j)*12 + c][ci] = w[c][ci][kt][i][j]; rows 108..111 zero.
-__global__ void head_prepare_kernel(const __nv_bfloat16* __restrict__ w, __nv_bfloat16* __restrict__ wp, int cin) {
-  const long long total = 3LL * CC_HEAD_G_CH * cin;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
-    const int ci = static_cast<int>(i % cin);
-    const long long r = i / cin;
-    const int row = static_cast<int>(r % CC_HEAD_G_CH);
-    const int kt = static_cast<int>(r / CC_HEAD_G_CH);
-    __nv_bfloat16 v = __float2bfloat16_rn(0.f);
-    if (row < 9 * CC_HEAD_COUT) {
-      const int c = row % CC_HEAD_COUT, tap = row / CC_HEAD_COUT;  // tap = i*3 + j
-      v = w[((long long)c * cin + ci) * 27 + kt * 9 + tap];
-    }
-    wp[i] = v;
   }
 }
 
@@ -215,63 +198,4 @@ extern "C" cc_status cc_resample_phase_conv(const cc_bf16* x, const cc_bf16* pw,
   a.out_batch = m * cout;
   a.bias = nullptr;
   return launch_tc_gemm<256, kAIm2col, false, false, false>(ta, tb, a, di, static_cast<cudaStream_t>(stream), what);
-}
-
-extern "C" cc_status cc_head_prepare(const cc_bf16* w, cc_bf16* wp, int cin, void* stream) {
-  cc_status st = check_ptrs("head_prepare", {w, wp});
-  if (st != CC_OK) return st;
-  if (cin <= 0) return fail(CC_ERR_INVALID, "head_prepare: C_in must be positive");
-  DeviceInfo di;
-  if ((st = device_info(&di)) != CC_OK) return st;
-  head_prepare_kernel<<<prep_grid(3LL * CC_HEAD_G_CH * cin), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const __nv_bfloat16*>(w), reinterpret_cast<__nv_bfloat16*>(wp), cin);
-  return launch_status("head_prepare");
-}
-
-extern "C" cc_status cc_head_temporal(const cc_bf16* x, const cc_bf16* wp, cc_bf16* g, int n, int d, int h, int w,
-                                      int cin, int hist, void* stream) {
-  const char* what = "head_temporal";
-  cc_status st = check_ptrs(what, {x, wp, g});
-  if (st != CC_OK) return st;
-  if ((st = check_grid(what, n, d, h, w, hist)) != CC_OK) return st;
-  if (cin <= 0 || cin % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C_in must be a positive multiple of 64", what);
-  DeviceInfo di;
-  if ((st = device_info(&di)) != CC_OK) return st;
-
-  const int lo_d = hist ? 0 : -2;
-  CUtensorMap ta, tb;
-  if ((st = encode_im2col_5d(&ta, x, n, d + hist, h, w, cin, -1, -1, lo_d, -1, -1, -2, kBlockM, kBlockK)) != CC_OK)
-    return st;
-  if ((st = encode_tiled_2d(&tb, wp, cin, 3ull * CC_HEAD_G_CH, 2ull * cin, kBlockK, CC_HEAD_G_CH)) != CC_OK) return st;
-
-  GemmArgs a{};
-  const long long m = (long long)n * d * h * w;
-  const long long plane = (long long)h * w;
-  a.m_total = static_cast<int>(m);
-  a.n_total = CC_HEAD_G_CH;
-  a.m_tiles = ceil_div(m, kBlockM);
-  a.n_tiles = 1;
-  a.batches = 1;
-  a.num_tiles = a.m_tiles;
-  a.taps = 3;
-  a.kb_per_tap = cin / kBlockK;
-  if (plane % kBlockM == 0) {  // walk the frames of one in-plane tile back to back
-    a.frame_tiles = static_cast<int>(plane / kBlockM);
-    a.frames = n * d;
-  }
-  a.img_w = w;
-  a.img_h = h;
-  a.img_d = d;
-  a.lo_w = -1;
-  a.lo_h = -1;
-  a.lo_d = lo_d;
-  for (int kt = 0; kt < 3; ++kt) a.tap_off[kt] = 1 | (1 << 8) | (kt << 16);
-  a.b_rows_per_tap = CC_HEAD_G_CH;
-  a.b_rows_per_batch = 0;
-  a.out = g;
-  a.out_ld = CC_HEAD_G_CH;
-  a.out_batch = 0;
-  a.bias = nullptr;
-  return launch_tc_gemm<CC_HEAD_G_CH, kAIm2col, false, false, false>(ta, tb, a, di, static_cast<cudaStream_t>(stream),
-                                                                      what);
 }

@@ -1,0 +1,339 @@
+// Output head, stage A: the temporal-only (3x1x1) part of conv_out, written as
+// g[n,t,p,(i*3+j)*12+c] = sum_{ci,kt} wp[kt][(i*3+j)*12+c][ci] x~[n,t+kt-2,p,ci]
+// (p = in-plane position), and the weight repack that feeds it.
+//
+// The operation is HBM-bound (a 256-channel input read once, 112 channels
+// written), so the kernel is organised around reading x exactly once:
+//  - the whole repacked weight (3 taps x 112 rows x C_in, 172 KB at C_in=256)
+//    is loaded into shared memory once per CTA and stays resident;
+//  - a CTA owns a 128-position in-plane tile of one image and walks its frames
+//    in order; each input frame tile (128 x C_in) is loaded once and feeds the
+//    three outputs that read it -- frame f is tap kt of output f - hist + 2 - kt
+//    -- through three of four TMEM accumulators (4 x 128 columns), so an
+//    output is complete, and drained by the epilogue warps, as soon as its
+//    last (kt = 2) frame has been multiplied in.
+// Warp 0 streams A with TMA, warp 1 issues tcgen05.mma (M=128, N=112, K=16),
+// warps 2-5 drain accumulators to bf16 g. Every wait is bounded.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "cc.h"
+#include "cc_gemm_launch.cuh"
+#include "cc_host.h"
+#include "cc_ptx.cuh"
+
+namespace cc {
+namespace {
+
+constexpr int kHeadN = CC_HEAD_G_CH;  // 112 output channels of stage A
+constexpr int kHeadAccCols = 128;     // TMEM columns per accumulator slot
+constexpr int kHeadSlots = 4;         // outputs t, t+1, t+2 accumulating + one draining
+constexpr int kSmemBudget = 232448;
+
+struct HeadArgs {
+  int plane;        // positions per frame (H*W)
+  int plane_tiles;  // 128-position tiles per frame
+  int units;        // images x plane tiles
+  int d_in;         // frames of x per image (D + hist)
+  int d_out;        // output frames per image
+  int hist;         // 0 or 2
+  __nv_bfloat16* g;
+  unsigned int* err;
+  unsigned long long timeout_ns;
+};
+
+template <int CB>  // C_in / 64
+struct HeadShape {
+  static constexpr int kBBlock = kHeadN * kBlockK * 2;  // one tap x 64 channels: 14,336 B
+  static constexpr int kBBytes = 3 * CB * kBBlock;
+  static constexpr int kABytes = kBlockM * kBlockK * 2;
+  static constexpr int kAStagesFit = (kSmemBudget - 1024 - 256 - kBBytes) / kABytes;
+  static constexpr int kAStages = kAStagesFit > 8 ? 8 : kAStagesFit;
+  static constexpr int kSmemBytes = 1024 + kBBytes + kAStages * kABytes + 256;
+  static_assert(kBBlock % 1024 == 0, "weight blocks must keep 1024-byte swizzle atoms aligned");
+  static_assert(kAStages >= 2, "at least two A stages");
+  static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
+};
+
+// First frame of x that contributes to output u.
+__device__ __forceinline__ int first_frame(int u, int hist) { return max(0, u + hist - 2); }
+
+template <int CB>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    head_temporal_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                         const __grid_constant__ HeadArgs a) {
+  using S = HeadShape<CB>;
+  constexpr int AST = S::kAStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sB = smem;
+  uint8_t* sA = smem + S::kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + AST * S::kABytes);
+  uint64_t* afull = bars;
+  uint64_t* aempty = bars + AST;
+  uint64_t* bfull = bars + 2 * AST;
+  uint64_t* tfull = bfull + 1;
+  uint64_t* tempty = tfull + kHeadSlots;
+  uint64_t* done = tempty + kHeadSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < AST; ++s) {
+      mbar_init(smem_u32(&afull[s]), 1);
+      mbar_init(smem_u32(&aempty[s]), 1);
+    }
+    mbar_init(smem_u32(bfull), 1);
+    for (int i = 0; i < kHeadSlots; ++i) {
+      mbar_init(smem_u32(&tfull[i]), 1);
+      mbar_init(smem_u32(&tempty[i]), 128);
+    }
+    mbar_init(smem_u32(done), 1);
+    fence_mbar_init();
+    tma_prefetch_map(&tmX);
+    tma_prefetch_map(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kHeadSlots * kHeadAccCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint64_t tlim = a.timeout_ns;
+
+  if (warp == 0) {
+    // ---------------------------------------------------- TMA producer --
+    if (lane == 0) {
+      const uint32_t bb = smem_u32(bfull);
+      mbar_arrive_expect_tx(bb, S::kBBytes);
+      for (int tap = 0; tap < 3; ++tap)
+        for (int kb = 0; kb < CB; ++kb)
+          tma_load_2d(smem_u32(sB + (tap * CB + kb) * S::kBBlock), &tmW, bb, kb * kBlockK, tap * kHeadN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; ok && unit < a.units; unit += gridDim.x) {
+        const int img = unit / a.plane_tiles;
+        const int m0 = (unit - img * a.plane_tiles) * kBlockM;
+        for (int f = 0; ok && f < a.d_in; ++f) {
+          for (int kb = 0; kb < CB; ++kb) {
+            if (!mbar_wait(smem_u32(&aempty[stage]), phase ^ 1u, a.err, tlim)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&afull[stage]);
+            mbar_arrive_expect_tx(fb, S::kABytes);
+            tma_load_3d(smem_u32(sA + stage * S::kABytes), &tmX, fb, kb * kBlockK, m0, img * a.d_in + f);
+            if (++stage == AST) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < AST; ++s)
+          (void)mbar_wait(smem_u32(&afull[s]), (s < stage) ? phase : (phase ^ 1u), a.err, 200000000ull);
+      }
+      (void)mbar_wait(bb, 0, a.err, 200000000ull);  // the weight copies have landed before any exit
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kHeadN, false);
+      bool ok = mbar_wait(smem_u32(bfull), 0, a.err, tlim);
+      tc_fence_after();
+      int stage = 0;
+      uint32_t phase = 0;
+      int q_base = 0;  // sequence number of this unit's output 0 among this CTA's outputs
+      for (int unit = blockIdx.x; ok && unit < a.units; unit += gridDim.x) {
+        for (int f = 0; ok && f < a.d_in; ++f) {
+          // Outputs this frame starts must have their accumulator slot drained.
+          for (int kt = 0; kt < 3; ++kt) {
+            const int u = f - a.hist + 2 - kt;
+            if (u < 0 || u >= a.d_out || f != first_frame(u, a.hist)) continue;
+            const int q = q_base + u;
+            if (!mbar_wait(smem_u32(&tempty[q & 3]), ((q >> 2) & 1) ^ 1u, a.err, tlim)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          tc_fence_after();
+          for (int kb = 0; kb < CB; ++kb) {
+            if (!mbar_wait(smem_u32(&afull[stage]), phase, a.err, tlim)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + stage * S::kABytes);
+#pragma unroll
+            for (int kt = 0; kt < 3; ++kt) {
+              const int u = f - a.hist + 2 - kt;
+              if (u < 0 || u >= a.d_out) continue;
+              const uint32_t d_tmem = tmem_base + ((q_base + u) & 3) * kHeadAccCols;
+              const bool first = (kb == 0) && (f == first_frame(u, a.hist));
+              const uint32_t b_addr = smem_u32(sB + (kt * CB + kb) * S::kBBlock);
+#pragma unroll
+              for (int k = 0; k < kBlockK / kUmmaK; ++k)
+                mma_bf16(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024), sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
+                         (first && k == 0) ? 0u : 1u);
+            }
+            mma_commit(smem_u32(&aempty[stage]));
+            if (++stage == AST) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          const int u_done = f - a.hist;  // its kt = 2 frame was the last one
+          if (u_done >= 0 && u_done < a.d_out) mma_commit(smem_u32(&tfull[(q_base + u_done) & 3]));
+        }
+        q_base += a.d_out;
+      }
+      mma_commit(smem_u32(done));
+      (void)mbar_wait(smem_u32(done), 0, a.err, tlim);
+    }
+  } else {
+    // -------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int q = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < a.units; unit += gridDim.x) {
+      const int img = unit / a.plane_tiles;
+      const int m = (unit - img * a.plane_tiles) * kBlockM + row;
+      const bool row_ok = m < a.plane;
+      for (int u = 0; u < a.d_out; ++u, ++q) {
+        const int slot = q & 3;
+        if (!mbar_wait(smem_u32(&tfull[slot]), (q >> 2) & 1, a.err, tlim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * kHeadAccCols;
+        __nv_bfloat16* out = a.g + ((long long)(img * a.d_out + u) * a.plane + m) * kHeadN;
+#pragma unroll 1
+        for (int c = 0; c < kHeadN; c += 16) {
+          uint32_t r[16];
+          __syncwarp();
+          tmem_ld16(tbase + c, r);
+          tmem_wait16(r);
+          if (row_ok) {
+            uint4 pk[2];
+            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) p2[j] = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            reinterpret_cast<uint4*>(out + c)[0] = pk[0];
+            reinterpret_cast<uint4*>(out + c)[1] = pk[1];
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&tempty[slot]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kHeadSlots * kHeadAccCols);
+  }
+}
+
+// wp[kt][(i*3+j)*12 + c][ci] = w[c][ci][kt][i][j]; rows 108..111 zero.
+__global__ void head_prepare_kernel(const __nv_bfloat16* __restrict__ w, __nv_bfloat16* __restrict__ wp, int cin) {
+  const long long total = 3LL * CC_HEAD_G_CH * cin;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const int ci = static_cast<int>(i % cin);
+    const long long r = i / cin;
+    const int row = static_cast<int>(r % CC_HEAD_G_CH);
+    const int kt = static_cast<int>(r / CC_HEAD_G_CH);
+    __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+    if (row < 9 * CC_HEAD_COUT) {
+      const int c = row % CC_HEAD_COUT, tap = row / CC_HEAD_COUT;  // tap = i*3 + j
+      v = w[((long long)c * cin + ci) * 27 + kt * 9 + tap];
+    }
+    wp[i] = v;
+  }
+}
+
+cc_status check_ptr(const char* what, const void* p) {
+  if (!p) return fail(CC_ERR_INVALID, "%s: null pointer", what);
+  if (!aligned16(p)) return fail(CC_ERR_INVALID, "%s: pointers must be 16-byte aligned", what);
+  return CC_OK;
+}
+
+template <int CB>
+cc_status launch_head_temporal(const CUtensorMap& tx, const CUtensorMap& tw, HeadArgs& a, const DeviceInfo& di,
+                               cudaStream_t stream) {
+  using S = HeadShape<CB>;
+  auto kern = head_temporal_kernel<CB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  if (e != cudaSuccess) return fail(CC_ERR_CUDA, "head_temporal: shared-memory attribute: %s", cudaGetErrorString(e));
+  a.err = di.err_word;
+  a.timeout_ns = kWaitLimitNs;
+  kern<<<std::min(a.units, di.sm_count), kGemmThreads, S::kSmemBytes, stream>>>(tx, tw, a);
+  return launch_status("head_temporal");
+}
+
+}  // namespace
+}  // namespace cc
+
+using namespace cc;
+
+extern "C" cc_status cc_head_prepare(const cc_bf16* w, cc_bf16* wp, int cin, void* stream) {
+  cc_status st;
+  if ((st = check_ptr("head_prepare", w)) != CC_OK || (st = check_ptr("head_prepare", wp)) != CC_OK) return st;
+  if (cin <= 0) return fail(CC_ERR_INVALID, "head_prepare: C_in must be positive");
+  DeviceInfo di;
+  if ((st = device_info(&di)) != CC_OK) return st;
+  const long long total = 3LL * CC_HEAD_G_CH * cin;
+  head_prepare_kernel<<<(unsigned)std::min<long long>((total + 255) / 256, 8192), 256, 0,
+                        static_cast<cudaStream_t>(stream)>>>(reinterpret_cast<const __nv_bfloat16*>(w),
+                                                             reinterpret_cast<__nv_bfloat16*>(wp), cin);
+  return launch_status("head_prepare");
+}
+
+extern "C" cc_status cc_head_temporal(const cc_bf16* x, const cc_bf16* wp, cc_bf16* g, int n, int d, int h, int w,
+                                      int cin, int hist, void* stream) {
+  const char* what = "head_temporal";
+  cc_status st;
+  if ((st = check_ptr(what, x)) != CC_OK || (st = check_ptr(what, wp)) != CC_OK || (st = check_ptr(what, g)) != CC_OK)
+    return st;
+  if (n <= 0 || d <= 0 || h <= 0 || w <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
+  if (hist != 0 && hist != 2) return fail(CC_ERR_INVALID, "%s: hist must be 0 or 2", what);
+  if (cin <= 0 || cin % 64 != 0 || cin > 256)
+    return fail(CC_ERR_UNSUPPORTED, "%s: C_in must be 64, 128, 192 or 256 (got %d)", what, cin);
+  const long long plane = (long long)h * w;
+  if (plane * n * (d + hist) > (1LL << 31) - 1) return fail(CC_ERR_UNSUPPORTED, "%s: too many positions", what);
+  DeviceInfo di;
+  if ((st = device_info(&di)) != CC_OK) return st;
+  CUtensorMap tx, tw;
+  // x as [frames = N*(D+hist)][plane][C_in]; rows past the plane are zero-filled
+  if ((st = encode_tiled_3d(&tx, x, cin, plane, (uint64_t)n * (d + hist), 2ull * cin, 2ull * cin * plane, kBlockK,
+                            kBlockM)) != CC_OK)
+    return st;
+  if ((st = encode_tiled_2d(&tw, wp, cin, 3ull * CC_HEAD_G_CH, 2ull * cin, kBlockK, CC_HEAD_G_CH)) != CC_OK) return st;
+  HeadArgs a{};
+  a.plane = static_cast<int>(plane);
+  a.plane_tiles = ceil_div(plane, kBlockM);
+  a.units = n * a.plane_tiles;
+  a.d_in = d + hist;
+  a.d_out = d;
+  a.hist = hist;
+  a.g = reinterpret_cast<__nv_bfloat16*>(g);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (cin / 64) {
+    case 1: return launch_head_temporal<1>(tx, tw, a, di, s);
+    case 2: return launch_head_temporal<2>(tx, tw, a, di, s);
+    case 3: return launch_head_temporal<3>(tx, tw, a, di, s);
+    default: return launch_head_temporal<4>(tx, tw, a, di, s);
+  }
+}

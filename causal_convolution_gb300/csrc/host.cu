@@ -138,6 +138,18 @@ cc_status encode_tiled_3d(CUtensorMap* map, const void* base, uint64_t d0, uint6
                        "3-D map");
 }
 
+cc_status encode_tiled_4d_dense(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides[3],
+                                uint32_t box0, uint32_t box1, uint32_t box2) {
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+  const cuuint32_t box[4] = {box0, box1, box2, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode_result(g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), d, st, box,
+                                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                       "4-D map");
+}
+
 // ------------------------------------------------------- self-test kernels --
 
 // One im2col load into a 1024-aligned shared tile, then every thread copies

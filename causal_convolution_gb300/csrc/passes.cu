@@ -8,6 +8,7 @@
 
 #include "cc.h"
 #include "cc_host.h"
+#include "cc_ptx.cuh"
 
 namespace cc {
 namespace {
@@ -81,57 +82,117 @@ __global__ void __launch_bounds__(256) interleave_kernel(const uint4* __restrict
   }
 }
 
-// One thread per output position: 12 fp32 accumulators start at the bias and
-// take channel block (i, j) of g from the neighbour (h+i-1, w+j-1), skipping
-// neighbours outside the plane; clamp, one bf16 rounding, 24-byte store.
-__global__ void __launch_bounds__(128) head_stencil_kernel(const __nv_bfloat16* __restrict__ g,
-                                                           const __nv_bfloat16* __restrict__ bias,
-                                                           __nv_bfloat16* __restrict__ out, int rows, int h, int w) {
-  float b[CC_HEAD_COUT];
+// Head stencil, persistent. A tile is 8 output rows x 32 output positions of
+// one frame; it needs the g window of rows h0-1 .. h0+8 and positions
+// w0-1 .. w0+32 with all 112 channels, which one rank-4 TMA box copies into
+// shared memory (zero-filled outside the plane, so the plane's zero padding
+// costs nothing). Each CTA walks tiles with a 3-deep ring of windows: while it
+// sums one tile, the next two are in flight. Three threads share an output
+// position, each summing 4 of its 12 channels over the nine (i, j) blocks
+// (8-byte shared reads), adding the bias, clamping and storing 8 bytes, so a
+// warp's stores form one contiguous run.
+constexpr int kStTW = 32;                                  // output positions per tile row
+constexpr int kStTH = 8;                                   // output rows per tile
+constexpr int kStPos = kStTW + 2;                          // positions held (with halo)
+constexpr int kStRows = kStTH + 2;                         // rows held (with halo)
+constexpr int kStBox = kStRows * kStPos * CC_HEAD_G_CH * 2;  // 76,160 bytes per window
+constexpr int kStStages = 3;
+constexpr int kStThreads = kStTW * kStTH * 3;
+constexpr int kStSmem = 1024 + kStStages * kStBox + 64;
+
+struct StencilArgs {
+  int h, w;
+  int strips, hblocks, tiles;
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* out;
+  unsigned int* err;
+  unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void stencil_tile_coords(const StencilArgs& a, int t, int& frame, int& hb, int& wb) {
+  wb = t % a.strips;
+  const int r = t / a.strips;
+  hb = r % a.hblocks;
+  frame = r / a.hblocks;
+}
+
+__global__ void __launch_bounds__(kStThreads, 1)
+    head_stencil_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ StencilArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStStages * kStBox);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < kStStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbar_init();
+    tma_prefetch_map(&tmG);
+  }
+  __syncthreads();
+
+  auto issue = [&](int t, int s) {
+    int frame, hb, wb;
+    stencil_tile_coords(a, t, frame, hb, wb);
+    const uint32_t bar = smem_u32(&full[s]);
+    mbar_arrive_expect_tx(bar, kStBox);
+    tma_load_4d(smem_u32(smem + s * kStBox), &tmG, bar, 0, wb * kStTW - 1, hb * kStTH - 1, frame);
+  };
+  // Tile iteration j of this CTA is tile blockIdx.x + j*gridDim.x, held in
+  // stage j % kStStages; its load is issued kStStages - 1 iterations early.
+  const int iters = (a.tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  if (tid == 0)
+    for (int j = 0; j < kStStages - 1 && j < iters; ++j) issue(blockIdx.x + j * gridDim.x, j);
+  const int cg = tid % 3;     // channels 4*cg .. 4*cg+3
+  const int pix = tid / 3;
+  const int p = pix % kStTW;
+  const int r = pix / kStTW;
+  float b4[4];
 #pragma unroll
-  for (int c = 0; c < CC_HEAD_COUT; ++c) b[c] = __bfloat162float(bias[c]);
-  for (int r = blockIdx.y; r < rows; r += gridDim.y) {
-    const int hh = r % h;
-    for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < w; x += gridDim.x * blockDim.x) {
-      float acc[CC_HEAD_COUT];
+  for (int e = 0; e < 4; ++e) b4[e] = __bfloat162float(a.bias[cg * 4 + e]);
+
+  int k = 0;
+  for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++k) {
+    const int stage = k % kStStages;
+    const bool ok = mbar_wait(smem_u32(&full[stage]), (k / kStStages) & 1, a.err, a.timeout_ns);
+    // one barrier per tile: every thread is done with tile k-1 here, so its
+    // window's stage may be refilled; a failed wait stops the whole CTA
+    if (__syncthreads_or(!ok)) break;
+    if (tid == 0 && k + kStStages - 1 < iters) issue(t + (kStStages - 1) * gridDim.x, (k + kStStages - 1) % kStStages);
+    int frame, hb, wb;
+    stencil_tile_coords(a, t, frame, hb, wb);
+    const int oh = hb * kStTH + r;
+    const int ow = wb * kStTW + p;
+    const uint8_t* win = smem + stage * kStBox;
+    float acc[4] = {b4[0], b4[1], b4[2], b4[3]};
 #pragma unroll
-      for (int c = 0; c < CC_HEAD_COUT; ++c) acc[c] = b[c];
+    for (int i = 0; i < 3; ++i) {
 #pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        const int gh = hh + i - 1;
-        if (gh < 0 || gh >= h) continue;
-        const long long grow = (long long)(r + i - 1) * w;
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          const int gw = x + j - 1;
-          if (gw < 0 || gw >= w) continue;
-          const uint2* src =
-              reinterpret_cast<const uint2*>(g + (grow + gw) * CC_HEAD_G_CH + (i * 3 + j) * CC_HEAD_COUT);
-#pragma unroll
-          for (int k = 0; k < 3; ++k) {
-            const uint2 u = __ldg(src + k);
-            const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
-            const float2 f0 = __bfloat1622float2(hv[0]);
-            const float2 f1 = __bfloat1622float2(hv[1]);
-            acc[4 * k] += f0.x;
-            acc[4 * k + 1] += f0.y;
-            acc[4 * k + 2] += f1.x;
-            acc[4 * k + 3] += f1.y;
-          }
-        }
-      }
-      uint2* dst = reinterpret_cast<uint2*>(out + ((long long)r * w + x) * CC_HEAD_COUT);
-#pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(fminf(1.f, fmaxf(-1.f, acc[4 * k])), fminf(1.f, fmaxf(-1.f, acc[4 * k + 1])));
-        __nv_bfloat162 hi =
-            __floats2bfloat162_rn(fminf(1.f, fmaxf(-1.f, acc[4 * k + 2])), fminf(1.f, fmaxf(-1.f, acc[4 * k + 3])));
-        uint2 u;
-        u.x = *reinterpret_cast<uint32_t*>(&lo);
-        u.y = *reinterpret_cast<uint32_t*>(&hi);
-        dst[k] = u;
+      for (int j = 0; j < 3; ++j) {
+        // g at (oh + i - 1, ow + j - 1) is held at row r + i, position p + j
+        const uint2 u = *reinterpret_cast<const uint2*>(
+            win + (((r + i) * kStPos + p + j) * CC_HEAD_G_CH + (i * 3 + j) * CC_HEAD_COUT + cg * 4) * 2);
+        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
+        const float2 f0 = __bfloat1622float2(hv[0]);
+        const float2 f1 = __bfloat1622float2(hv[1]);
+        acc[0] += f0.x;
+        acc[1] += f0.y;
+        acc[2] += f1.x;
+        acc[3] += f1.y;
       }
     }
+    if (oh < a.h && ow < a.w) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(fminf(1.f, fmaxf(-1.f, acc[0])), fminf(1.f, fmaxf(-1.f, acc[1])));
+      __nv_bfloat162 hi = __floats2bfloat162_rn(fminf(1.f, fmaxf(-1.f, acc[2])), fminf(1.f, fmaxf(-1.f, acc[3])));
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(a.out + (((long long)frame * a.h + oh) * a.w + ow) * CC_HEAD_COUT + cg * 4) = u;
+    }
+  }
+  if (tid == 0) {
+    // after a failed wait, let the copies still in flight (iterations k ..
+    // k + kStStages - 2) land before the CTA exits
+    for (int j = k; j < iters && j < k + kStStages - 1; ++j)
+      (void)mbar_wait(smem_u32(&full[j % kStStages]), (j / kStStages) & 1, a.err, 200000000ull);
   }
 }
 
@@ -202,17 +263,29 @@ extern "C" cc_status cc_head_stencil(const cc_bf16* g, const cc_bf16* bias, cc_b
       (st = check_ptr(what, out)) != CC_OK)
     return st;
   if (n <= 0 || d <= 0 || h <= 0 || w <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
-  const long long rows = (long long)n * d * h;
-  if (rows > (1LL << 31) - 1 || (long long)rows * w > (1LL << 40))
+  const long long frames = (long long)n * d;
+  const long long strips = (w + kStTW - 1) / kStTW, hblocks = (h + kStTH - 1) / kStTH;
+  if (frames * strips * hblocks > (1LL << 31) - 1 || frames * h * w > (1LL << 40))
     return fail(CC_ERR_UNSUPPORTED, "%s: tensor too large", what);
   DeviceInfo di;
   if ((st = device_info(&di)) != CC_OK) return st;
-  const int threads = 128;
-  const unsigned gx = (unsigned)std::min<long long>((w + threads - 1) / threads, 65535);
-  const unsigned gy = (unsigned)std::min<long long>(rows, 65535);
-  head_stencil_kernel<<<dim3(gx, gy), threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const __nv_bfloat16*>(g), reinterpret_cast<const __nv_bfloat16*>(bias),
-      reinterpret_cast<__nv_bfloat16*>(out), (int)rows, h, w);
+  CUtensorMap tm;
+  const uint64_t dims[4] = {CC_HEAD_G_CH, (uint64_t)w, (uint64_t)h, (uint64_t)frames};
+  const uint64_t strides[3] = {CC_HEAD_G_CH * 2ull, CC_HEAD_G_CH * 2ull * w, CC_HEAD_G_CH * 2ull * w * h};
+  if ((st = encode_tiled_4d_dense(&tm, g, dims, strides, CC_HEAD_G_CH, kStPos, kStRows)) != CC_OK) return st;
+  StencilArgs a{};
+  a.h = h;
+  a.w = w;
+  a.strips = (int)strips;
+  a.hblocks = (int)hblocks;
+  a.tiles = (int)(frames * strips * hblocks);
+  a.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
+  a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.err = di.err_word;
+  a.timeout_ns = kWaitLimitNs;
+  cudaError_t e = cudaFuncSetAttribute(head_stencil_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStSmem);
+  if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: shared-memory attribute: %s", what, cudaGetErrorString(e));
+  head_stencil_kernel<<<std::min(a.tiles, di.sm_count), kStThreads, kStSmem, static_cast<cudaStream_t>(stream)>>>(tm, a);
   return launch_status(what);
 }
 
