@@ -154,7 +154,9 @@ extern "C" cc_status cc_attn_scores(const cc_bf16* q, const cc_bf16* k, float* s
   if ((st = device_info(&di)) != CC_OK) return st;
   CUtensorMap ta, tb;
   if ((st = encode_tiled_3d(&ta, q, c, hw, t, 2ull * ld_q, 2ull * ld_q * hw, kBlockK, kBlockM)) != CC_OK) return st;
-  if ((st = encode_tiled_3d(&tb, k, c, hw, t, 2ull * ld_k, 2ull * ld_k * hw, kBlockK, 256)) != CC_OK) return st;
+  const bool pair = hw > kBlockM;
+  if ((st = encode_tiled_3d(&tb, k, c, hw, t, 2ull * ld_k, 2ull * ld_k * hw, kBlockK, pair ? 128 : 256)) != CC_OK)
+    return st;
   GemmArgs a{};
   a.m_total = hw;
   a.n_total = hw;
@@ -167,7 +169,9 @@ extern "C" cc_status cc_attn_scores(const cc_bf16* q, const cc_bf16* k, float* s
   a.out = s;
   a.out_ld = ld_s;
   a.out_batch = (long long)hw * ld_s;
-  return launch_tc_gemm<256, kATiled3d, false, true, false>(ta, tb, a, di, static_cast<cudaStream_t>(stream), what);
+  cudaStream_t s_ = static_cast<cudaStream_t>(stream);
+  if (pair) return launch_tc_gemm_pair<256, kATiled3d, false, true, false>(ta, tb, a, di, s_, what);
+  return launch_tc_gemm<256, kATiled3d, false, true, false>(ta, tb, a, di, s_, what);
 }
 
 extern "C" cc_status cc_attn_softmax(const float* s, cc_bf16* p, int t, int hw, int64_t ld_s, int64_t ld_p,
@@ -230,7 +234,9 @@ extern "C" cc_status cc_attn_pv(const cc_bf16* p, const cc_bf16* v, cc_bf16* o, 
   a.out = o;
   a.out_ld = ld_o;
   a.out_batch = (long long)hw * ld_o;
-  return launch_tc_gemm<256, kATiled3d, true, false, false>(ta, tb, a, di, static_cast<cudaStream_t>(stream), what);
+  cudaStream_t s_ = static_cast<cudaStream_t>(stream);
+  if (hw > kBlockM) return launch_tc_gemm_pair<256, kATiled3d, true, false, false>(ta, tb, a, di, s_, what);
+  return launch_tc_gemm<256, kATiled3d, true, false, false>(ta, tb, a, di, s_, what);
 }
 
 extern "C" cc_status cc_attn_frame(const cc_bf16* q, const cc_bf16* k, const cc_bf16* v, cc_bf16* o, int t, int hw,

@@ -4,6 +4,7 @@
 #include <algorithm>
 
 #include "cc_gemm.cuh"
+#include "cc_gemm_pair.cuh"
 #include "cc_host.h"
 
 namespace cc {
@@ -20,6 +21,24 @@ cc_status launch_tc_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs&
   args.timeout_ns = kWaitLimitNs;
   const int grid = std::min(args.num_tiles, di.sm_count);
   kern<<<grid, kGemmThreads, S::kSmemBytes, stream>>>(ta, tb, args);
+  return launch_status(what);
+}
+
+// Pair kernel: args.m_tiles counts 128-row tiles; args.num_tiles is
+// overwritten with the number of 256-row pair tiles.
+template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS>
+cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs& args, const DeviceInfo& di,
+                              cudaStream_t stream, const char* what) {
+  using S = PairShape<BN>;
+  args.num_tiles = ((args.m_tiles + 1) / 2) * args.n_tiles * args.batches;
+  if (args.num_tiles <= 0) return CC_OK;
+  auto kern = tc_gemm_pair_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: shared-memory attribute: %s", what, cudaGetErrorString(e));
+  args.err = di.err_word;
+  args.timeout_ns = kWaitLimitNs;
+  const int pairs = std::min(args.num_tiles, di.sm_count / 2);
+  kern<<<2 * pairs, kGemmThreads, S::kSmemBytes, stream>>>(ta, tb, args);
   return launch_status(what);
 }
 

@@ -1,0 +1,302 @@
+// The same implicit GEMM on CTA pairs: one tcgen05.mma.cta_group::2 computes
+// a 256 x BN tile across two SMs. CTA rank r of the pair streams its own A
+// tile (rows 128r .. 128r+127 of the pair tile) and its half of B (BN/2 rows)
+// into its own shared memory; the even CTA's single MMA thread reads both
+// CTAs' operands and writes each CTA's 128 accumulator rows into that CTA's
+// TMEM. Per k-block each SM now loads 16 KB of A and 16 KB of B for a 128 x BN
+// share of the tile (the single-CTA kernel loads 16 KB + 32 KB), which lowers
+// both the L2 traffic and the shared-memory reads per MMA.
+//
+// Synchronisation across the pair: both producers complete their copies on
+// the even CTA's `full` barrier (the even producer alone declares the bytes
+// of both); MMA completion is multicast to the `empty` / `tfull` barriers of
+// both CTAs; both epilogues arrive on the even CTA's `tempty`. Every wait is
+// bounded, and a cluster barrier at the end keeps each CTA's shared memory
+// alive until its peer is done with it.
+#pragma once
+
+#include "cc_gemm.cuh"
+
+namespace cc {
+
+template <int BN>
+struct PairShape {
+  static constexpr int kHalfN = BN / 2;
+  static constexpr int kABytes = kBlockM * kBlockK * 2;
+  static constexpr int kBBytes = kHalfN * kBlockK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;  // per CTA
+  static constexpr int kStagesFit = (232448 - 1024 - 256) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr uint32_t kAccCols = BN <= 128 ? 128 : 256;
+  static constexpr uint32_t kTmemCols = 2 * kAccCols;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  static_assert(BN % 128 == 0 && BN <= 256, "pair tiles split B into halves of whole 64-column blocks");
+  static_assert(kBBytes % 1024 == 0, "B stage must be a whole number of 1024-byte swizzle atoms");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// tile -> (batch, pair row tile, column tile); the CTA of rank r takes row
+// tile 2 * mp + r.
+__device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, int& batch, int& mp, int& nt) {
+  nt = tile % a.n_tiles;
+  const int r = tile / a.n_tiles;
+  batch = r % a.batches;
+  mp = r / a.batches;
+}
+
+template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ GemmArgs args) {
+  using S = PairShape<BN>;
+  constexpr int STAGES = S::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * S::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * S::kBBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&tfull[i]), 1);
+      mbar_init(smem_u32(&tempty[i]), 2 * 128);
+    }
+    mbar_init(smem_u32(done), 1);
+    fence_mbar_init();
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), S::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint64_t tlim = args.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
+        int batch, mp, nt;
+        pair_decode_tile(args, tile, batch, mp, nt);
+        const int m0 = (2 * mp + static_cast<int>(rank)) * kBlockM;
+        const int nb0 = nt * BN + static_cast<int>(rank) * S::kHalfN;  // this CTA's half of the columns
+        int cw = 0, ch = 0, cd = 0, cn = 0;
+        if (AMODE == kAIm2col) {
+          int q = m0;
+          cw = q % args.img_w;
+          q /= args.img_w;
+          ch = q % args.img_h;
+          q /= args.img_h;
+          cd = q % args.img_d;
+          cn = q / args.img_d;
+          cw += args.lo_w;
+          ch += args.lo_h;
+          cd += args.lo_d;
+        }
+        for (int tap = 0; ok && tap < args.taps; ++tap) {
+          const int off = (AMODE == kAIm2col) ? args.tap_off[batch * args.taps + tap] : 0;
+          const int brow = batch * args.b_rows_per_batch + tap * args.b_rows_per_tap + nb0;
+          for (int kb = 0; kb < args.kb_per_tap; ++kb) {
+            if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, args.err, tlim)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb_local = smem_u32(&full[stage]);
+            const uint32_t fb = mapa_shared(fb_local, 0);
+            if (leader) mbar_arrive_expect_tx(fb_local, 2 * S::kStageBytes);
+            const uint32_t dA = smem_u32(sA + stage * S::kABytes);
+            const uint32_t dB = smem_u32(sB + stage * S::kBBytes);
+            if (AMODE == kAIm2col) {
+              tma_load_im2col_5d_pair(dA, &tmA, fb, kb * kBlockK, cw, ch, cd, cn, uint16_t(off & 0xff),
+                                      uint16_t((off >> 8) & 0xff), uint16_t((off >> 16) & 0xff));
+              tma_load_2d_pair(dB, &tmB, fb, kb * kBlockK, brow);
+            } else {
+              tma_load_3d_pair(dA, &tmA, fb, kb * kBlockK, m0, batch);
+              if (B_MN) {
+#pragma unroll
+                for (int j = 0; j < S::kHalfN / 64; ++j)
+                  tma_load_3d_pair(dB + j * 8192, &tmB, fb, nb0 + 64 * j, kb * kBlockK, batch);
+              } else {
+                tma_load_3d_pair(dB, &tmB, fb, kb * kBlockK, nb0, batch);
+              }
+            }
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok && leader) {
+        // copies of both CTAs complete on the even CTA's barriers; let the
+        // armed ones land (200 ms each at most) before the pair winds down
+        for (int s = 0; s < STAGES; ++s)
+          (void)mbar_wait(smem_u32(&full[s]), (s < stage) ? phase : (phase ^ 1u), args.err, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------- MMA issuer (even CTA only) --
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBlockM, BN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const int kblocks = args.taps * args.kb_per_tap;
+      for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
+        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, args.err, tlim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * S::kAccCols;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, args.err, tlim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * S::kABytes);
+          const uint32_t b_addr = smem_u32(sB + stage * S::kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+            const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b_addr + k * 2048, 8192, 1024) : sdesc_sw128(b_addr + k * 32, 16, 1024);
+            mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit_pair_both(smem_u32(&empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_both(smem_u32(&tfull[acc]));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      mma_commit_pair_both(smem_u32(done));
+      (void)mbar_wait(smem_u32(done), 0, args.err, tlim);
+    }
+  } else {
+    // --------------------------------------------- epilogue (both CTAs) --
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < args.num_tiles; tile += npairs) {
+      int batch, mp, nt;
+      pair_decode_tile(args, tile, batch, mp, nt);
+      if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim)) break;
+      tc_fence_after();
+      const int m = (2 * mp + static_cast<int>(rank)) * kBlockM + row;
+      const int n0 = nt * BN;
+      const bool row_ok = m < args.m_total;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * S::kAccCols;
+      const long long roff = static_cast<long long>(batch) * args.out_batch + static_cast<long long>(m) * args.out_ld;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        uint32_t r[16];
+        __syncwarp();
+        tmem_ld16(tbase + c, r);
+        tmem_wait16(r);
+        const int n = n0 + c;
+        if (!row_ok || n >= args.n_total) continue;
+        const bool full_chunk = n + 16 <= args.n_total;
+        if (OUT_F32) {
+          float* o = static_cast<float*>(args.out) + roff + n;
+          if (full_chunk) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              reinterpret_cast<float4*>(o)[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (n + j < args.n_total) o[j] = __uint_as_float(r[j]);
+          }
+        } else {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+          if (HAS_BIAS) {
+            if (full_chunk) {
+              const uint4* bp = reinterpret_cast<const uint4*>(args.bias + n);
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                uint4 bb = __ldg(bp + hh);
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bb);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  float2 f = __bfloat1622float2(b2[j]);
+                  v[8 * hh + 2 * j] += f.x;
+                  v[8 * hh + 2 * j + 1] += f.y;
+                }
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (n + j < args.n_total) v[j] += __bfloat162float(args.bias[n + j]);
+            }
+          }
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) + roff + n;
+          if (full_chunk) {
+            uint4 pk[2];
+            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) p2[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+            reinterpret_cast<uint4*>(o)[0] = pk[0];
+            reinterpret_cast<uint4*>(o)[1] = pk[1];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (n + j < args.n_total) o[j] = __float2bfloat16_rn(v[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer no longer reads this CTA's shared memory or signals its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, S::kTmemCols);
+  }
+}
+
+}  // namespace cc

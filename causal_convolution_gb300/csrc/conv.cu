@@ -105,10 +105,13 @@ extern "C" cc_status cc_conv3d_causal(const cc_bf16* x, const cc_bf16* wp, const
   CUtensorMap ta, tb;
   if ((st = encode_im2col_5d(&ta, x, n, d + hist, h, w, cin, -1, -1, lo_d, -1, -1, -2, kBlockM, kBlockK)) != CC_OK)
     return st;
-  if ((st = encode_tiled_2d(&tb, wp, cin, 27ull * cout, 2ull * cin, kBlockK, 256)) != CC_OK) return st;
+  const long long m = (long long)n * d * h * w;
+  // two or more 128-row tiles: 256 x 256 tiles on CTA pairs, each CTA
+  // loading half of B (128 rows per box)
+  const bool pair = m > kBlockM;
+  if ((st = encode_tiled_2d(&tb, wp, cin, 27ull * cout, 2ull * cin, kBlockK, pair ? 128 : 256)) != CC_OK) return st;
 
   GemmArgs a{};
-  const long long m = (long long)n * d * h * w;
   a.m_total = static_cast<int>(m);
   a.n_total = cout;
   a.m_tiles = ceil_div(m, kBlockM);
@@ -133,6 +136,10 @@ extern "C" cc_status cc_conv3d_causal(const cc_bf16* x, const cc_bf16* wp, const
   a.out_batch = 0;
   a.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pair) {
+    if (bias) return launch_tc_gemm_pair<256, kAIm2col, false, false, true>(ta, tb, a, di, s, what);
+    return launch_tc_gemm_pair<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
+  }
   if (bias) return launch_tc_gemm<256, kAIm2col, false, false, true>(ta, tb, a, di, s, what);
   return launch_tc_gemm<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
 }
@@ -164,10 +171,11 @@ extern "C" cc_status cc_resample_phase_conv(const cc_bf16* x, const cc_bf16* pw,
   CUtensorMap ta, tb;
   if ((st = encode_im2col_5d(&ta, x, n, d + hist, hl, wl, cin, -1, -1, lo_d, -1, -1, -2, kBlockM, kBlockK)) != CC_OK)
     return st;
-  if ((st = encode_tiled_2d(&tb, pw, cin, 48ull * cout, 2ull * cin, kBlockK, 256)) != CC_OK) return st;
+  const long long m = (long long)n * d * hl * wl;
+  const bool pair = m > kBlockM;
+  if ((st = encode_tiled_2d(&tb, pw, cin, 48ull * cout, 2ull * cin, kBlockK, pair ? 128 : 256)) != CC_OK) return st;
 
   GemmArgs a{};
-  const long long m = (long long)n * d * hl * wl;
   a.m_total = static_cast<int>(m);
   a.n_total = cout;
   a.m_tiles = ceil_div(m, kBlockM);
@@ -197,5 +205,7 @@ extern "C" cc_status cc_resample_phase_conv(const cc_bf16* x, const cc_bf16* pw,
   a.out_ld = cout;
   a.out_batch = m * cout;
   a.bias = nullptr;
-  return launch_tc_gemm<256, kAIm2col, false, false, false>(ta, tb, a, di, static_cast<cudaStream_t>(stream), what);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pair) return launch_tc_gemm_pair<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
+  return launch_tc_gemm<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
 }
