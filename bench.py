@@ -40,8 +40,13 @@ METRIC = "causal-conv TFLOP/s (% of bf16 peak); resampler HBM GB/s; ms per 4-fra
 WORKLOAD = ("one 4-latent-frame chunk through the four stages: causal conv 1024->1024 @ 4x44x78; "
             "attention 4x3432xC1024; resampler 512->512 @ 8x88x156 -> 8x176x312; head 256->12 @ 16x352x624")
 
-KERNELS = ["conv3d_causal", "attn_scores", "attn_softmax", "attn_pv", "resample_phase_conv",
-           "resample_interleave", "head_temporal", "head_stencil"]
+# The step: every row of the hot path, with the resampler's phase convs and
+# interleave (rows a4, a5) fused into one kernel.
+KERNELS = ["conv3d_causal", "attn_scores", "attn_softmax", "attn_pv", "resample_up2_fused", "head_temporal",
+           "head_stencil"]
+# Rows a4 and a5 as the two separate passes of the reference design, timed in
+# their own loop after the step (not part of the step's time).
+ROW_KERNELS = ["resample_phase_conv", "resample_interleave"]
 
 
 def algorithmic_work():
@@ -61,6 +66,7 @@ def algorithmic_work():
         "attn_softmax": ("hbm", t * hw * hw * 4.0 + t * hw * ld * 2.0, "byte"),
         "attn_pv": ("tensor", 2.0 * t * hw * hw * c, "flop"),
         "resample_phase_conv": ("tensor", 2.0 * 4 * m_res * rs.cout * 12 * rs.c, "flop"),
+        "resample_up2_fused": ("tensor", 2.0 * 4 * m_res * rs.cout * 12 * rs.c, "flop"),
         "resample_interleave": ("hbm", (4 + 1 + 4) * m_res * rs.c * 2.0, "byte"),
         "head_temporal": ("hbm", m_head * hd.c * 2.0 + m_head * 112 * 2.0, "byte"),
         "head_stencil": ("hbm", m_head * 112 * 2.0 + m_head * 12 * 2.0, "byte"),
@@ -72,6 +78,7 @@ _GEMM_SRC = ["csrc/cc_gemm.cuh", "csrc/cc_ptx.cuh", "csrc/cc_gemm_launch.cuh", "
 KERNEL_SOURCES = {
     "conv3d_causal": _GEMM_SRC + ["csrc/conv.cu"],
     "resample_phase_conv": _GEMM_SRC + ["csrc/conv.cu"],
+    "resample_up2_fused": _GEMM_SRC + ["csrc/conv.cu"],
     "head_temporal": _GEMM_SRC + ["csrc/head.cu"],
     "attn_scores": _GEMM_SRC + ["csrc/attn.cu"],
     "attn_pv": _GEMM_SRC + ["csrc/attn.cu"],
@@ -232,7 +239,7 @@ class Workload:
         api.cc_check_device()
 
     def step(self, stream, ev=None):
-        """The whole hot path once. With `ev` (9 events) each launch is bracketed."""
+        """The whole hot path once. With `ev` (len(KERNELS)+1 events) each launch is bracketed."""
         a = self.api
         rec = (lambda j: ev[j].record(stream)) if ev is not None else (lambda j: None)
         rec(0)
@@ -244,14 +251,21 @@ class Workload:
         rec(3)
         a.cc_attn_pv(self.p, self.v, self.o, self.at.hw, stream=stream)
         rec(4)
-        a.cc_resample_phase_conv(self.res_x, self.res_pw, self.phases, stream=stream)
+        a.cc_resample_up2_fused(self.res_x, self.res_pw, self.res_b, self.res_skip, self.res_out, stream=stream)
         rec(5)
-        a.cc_resample_interleave(self.phases, self.res_b, self.res_skip, self.res_out, stream=stream)
-        rec(6)
         a.cc_head_temporal(self.head_x, self.head_wp, self.g, stream=stream)
-        rec(7)
+        rec(6)
         a.cc_head_stencil(self.g, self.head_b, self.head_out, stream=stream)
-        rec(8)
+        rec(7)
+
+    def rows(self, stream, ev):
+        """Rows a4 and a5 as two passes through the phase tensors (3 events)."""
+        a = self.api
+        ev[0].record(stream)
+        a.cc_resample_phase_conv(self.res_x, self.res_pw, self.phases, stream=stream)
+        ev[1].record(stream)
+        a.cc_resample_interleave(self.phases, self.res_b, self.res_skip, self.res_out, stream=stream)
+        ev[2].record(stream)
 
     # ---- end to end through host buffers -------------------------------
     def host_buffers(self):
@@ -449,7 +463,7 @@ def main(argv=None):
     torch.cuda.synchronize(device)
     wl.api.cc_check_device()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -472,6 +486,17 @@ def main(argv=None):
                   for j, name in enumerate(KERNELS)}
     ms_step = max_over_ranks(elapsed / args.steps, device)
 
+    # the resampler's two-pass form (rows a4, a5), outside the step
+    rev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for _ in range(2):
+        wl.rows(stream, rev[0])
+    for k in range(args.steps):
+        wl.rows(stream, rev[k])
+    torch.cuda.synchronize(device)
+    for j, name in enumerate(ROW_KERNELS):
+        per_kernel[name] = float(np.mean([rev[k][j].elapsed_time(rev[k][j + 1]) for k in range(args.steps)]))
+    wl.api.cc_check_device()
+
     # end to end: host buffers, copies inside the timed region
     h2d, d2h = wl.host_buffers()
     wl.step_e2e(stream)
@@ -488,19 +513,19 @@ def main(argv=None):
     peaks = load_peaks()
     work = algorithmic_work()
     roofs = {}
-    for name in KERNELS:
+    for name in KERNELS + ROW_KERNELS:
         bound, amount, unit = work[name]
         sec = per_kernel[name] * 1e-3
         if bound == "tensor":
             ach = amount / sec / 1e12
             peak = peaks["bf16_tflops"]
             roofs[name] = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
-                           "ms": per_kernel[name], "work": amount}
+                           "ms": per_kernel[name], "work": amount, "in_step": name in KERNELS}
         else:
             ach = amount / sec / 1e9
             peak = peaks["hbm_gbs"]
             roofs[name] = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                           "ms": per_kernel[name], "work": amount}
+                           "ms": per_kernel[name], "work": amount, "in_step": name in KERNELS}
     dominant = max(KERNELS, key=lambda n: per_kernel[n])
     dr = roofs[dominant]
     traffic = measured_traffic()
@@ -520,9 +545,11 @@ def main(argv=None):
         "head_stencil_gbs": round(roofs["head_stencil"]["achieved"], 1),
         "stage_ms": {"conv": per_kernel["conv3d_causal"],
                      "attention": per_kernel["attn_scores"] + per_kernel["attn_softmax"] + per_kernel["attn_pv"],
-                     "resampler": per_kernel["resample_phase_conv"] + per_kernel["resample_interleave"],
+                     "resampler": per_kernel["resample_up2_fused"],
+                     "resampler_two_pass": per_kernel["resample_phase_conv"] + per_kernel["resample_interleave"],
                      "head": per_kernel["head_temporal"] + per_kernel["head_stencil"]},
-        "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()} for n, r in roofs.items()},
+        "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
+                    for n, r in roofs.items()},
         "roofline": roofline,
         "e2e": {"value": round(e2e_ms / ws, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": len(KERNELS) * args.steps,

@@ -57,6 +57,7 @@ struct GemmArgs {
   long long out_ld;      // elements between rows
   long long out_batch;   // elements between batches
   const __nv_bfloat16* bias;  // per column, or nullptr
+  const __nv_bfloat16* skip;  // resampler epilogue: shortcut rows (row m at m * out_ld)
   unsigned int* err;
   unsigned long long timeout_ns;
 };
@@ -89,7 +90,87 @@ __device__ __forceinline__ void gemm_decode_tile(const GemmArgs& a, int tile, in
   }
 }
 
-template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS>
+// Epilogue modes. Plain: row m of batch b goes to out + b*out_batch + m*out_ld.
+// Resample: the accumulator rows are low-resolution positions (frame f, row i,
+// column j) of output parity batch = 2p + q; the row is written, with the bias
+// and the shortcut row m added, to high-resolution position (f, 2i+p, 2j+q) of
+// out [frames, 2*img_h, 2*img_w, out_ld] -- the interleave done in registers.
+enum EpiMode : int { kEpiPlain = 0, kEpiResample = 1 };
+
+template <int EPI>
+__device__ __forceinline__ long long epi_row_offset(const GemmArgs& a, int batch, int m) {
+  if (EPI == kEpiResample) {
+    const int j = m % a.img_w;
+    const int r = m / a.img_w;
+    const int i = r % a.img_h;
+    const long long f = r / a.img_h;
+    const int p = batch >> 1, q = batch & 1;
+    return ((f * (2 * a.img_h) + 2 * i + p) * (2LL * a.img_w) + 2 * j + q) * a.out_ld;
+  }
+  return static_cast<long long>(batch) * a.out_batch + static_cast<long long>(m) * a.out_ld;
+}
+
+__device__ __forceinline__ void add_bf16x16(float (&v)[16], const __nv_bfloat16* src) {
+  const uint4* sp = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 bb = __ldg(sp + h);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bb);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(b2[j]);
+      v[8 * h + 2 * j] += f.x;
+      v[8 * h + 2 * j + 1] += f.y;
+    }
+  }
+}
+
+// Stores accumulator columns n .. n+15 (r) of one row at element offset roff
+// (skip row at soff): + bias, + shortcut, one rounding (or fp32 as is).
+template <bool OUT_F32, bool HAS_BIAS, int EPI>
+__device__ __forceinline__ void epi_store16(const GemmArgs& a, long long roff, long long soff, int n,
+                                            const uint32_t (&r)[16]) {
+  const bool full_chunk = n + 16 <= a.n_total;
+  if constexpr (OUT_F32) {
+    float* o = static_cast<float*>(a.out) + roff + n;
+    if (full_chunk) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        reinterpret_cast<float4*>(o)[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (n + j < a.n_total) o[j] = __uint_as_float(r[j]);
+    }
+  } else {
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + roff + n;
+  if (full_chunk) {
+    if (HAS_BIAS) add_bf16x16(v, a.bias + n);
+    if (EPI == kEpiResample) add_bf16x16(v, a.skip + soff + n);
+    uint4 pk[2];
+    __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) p2[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+    reinterpret_cast<uint4*>(o)[0] = pk[0];
+    reinterpret_cast<uint4*>(o)[1] = pk[1];
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (n + j >= a.n_total) continue;
+      float t = v[j];
+      if (HAS_BIAS) t += __bfloat162float(a.bias[n + j]);
+      if (EPI == kEpiResample) t += __bfloat162float(a.skip[soff + n + j]);
+      o[j] = __float2bfloat16_rn(t);
+    }
+  }
+  }
+}
+
+template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = kEpiPlain>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs args) {
@@ -261,13 +342,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
       int batch, mt, nt;
       gemm_decode_tile(args, tile, batch, mt, nt);
-      if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim)) break;
+      // warp-uniform: the lanes leave together (they share .sync.aligned ops)
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
       tc_fence_after();
       const int m = mt * kBlockM + row;
       const int n0 = nt * BN;
       const bool row_ok = m < args.m_total;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * S::kAccCols;
-      const long long roff = static_cast<long long>(batch) * args.out_batch + static_cast<long long>(m) * args.out_ld;
+      const long long roff = row_ok ? epi_row_offset<EPI>(args, batch, m) : 0;
+      const long long soff = static_cast<long long>(m) * args.out_ld;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 16) {
         uint32_t r[16];
@@ -275,58 +358,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_ld16(tbase + c, r);
         tmem_wait16(r);
         const int n = n0 + c;
-        if (!row_ok || n >= args.n_total) continue;
-        const bool full_chunk = n + 16 <= args.n_total;
-        if (OUT_F32) {
-          float* o = static_cast<float*>(args.out) + roff + n;
-          if (full_chunk) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              reinterpret_cast<float4*>(o)[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (n + j < args.n_total) o[j] = __uint_as_float(r[j]);
-          }
-        } else {
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-          if (HAS_BIAS) {
-            if (full_chunk) {
-              const uint4* bp = reinterpret_cast<const uint4*>(args.bias + n);
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                uint4 bb = __ldg(bp + h);
-                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bb);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  float2 f = __bfloat1622float2(b2[j]);
-                  v[8 * h + 2 * j] += f.x;
-                  v[8 * h + 2 * j + 1] += f.y;
-                }
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (n + j < args.n_total) v[j] += __bfloat162float(args.bias[n + j]);
-            }
-          }
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) + roff + n;
-          if (full_chunk) {
-            uint4 pk[2];
-            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) p2[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-            reinterpret_cast<uint4*>(o)[0] = pk[0];
-            reinterpret_cast<uint4*>(o)[1] = pk[1];
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (n + j < args.n_total) o[j] = __float2bfloat16_rn(v[j]);
-          }
-        }
+        if (row_ok && n < args.n_total) epi_store16<OUT_F32, HAS_BIAS, EPI>(args, roff, soff, n, r);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[acc]));

@@ -9,12 +9,12 @@
 
 namespace cc {
 
-template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS>
+template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = kEpiPlain>
 cc_status launch_tc_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs& args, const DeviceInfo& di,
                          cudaStream_t stream, const char* what) {
   using S = GemmShape<BN>;
   if (args.num_tiles <= 0) return CC_OK;
-  auto kern = tc_gemm_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS>;
+  auto kern = tc_gemm_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: shared-memory attribute: %s", what, cudaGetErrorString(e));
   args.err = di.err_word;
@@ -26,13 +26,13 @@ cc_status launch_tc_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs&
 
 // Pair kernel: args.m_tiles counts 128-row tiles; args.num_tiles is
 // overwritten with the number of 256-row pair tiles.
-template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS>
+template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = kEpiPlain>
 cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs& args, const DeviceInfo& di,
                               cudaStream_t stream, const char* what) {
   using S = PairShape<BN>;
   args.num_tiles = ((args.m_tiles + 1) / 2) * args.n_tiles * args.batches;
   if (args.num_tiles <= 0) return CC_OK;
-  auto kern = tc_gemm_pair_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS>;
+  auto kern = tc_gemm_pair_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: shared-memory attribute: %s", what, cudaGetErrorString(e));
   args.err = di.err_word;

@@ -44,7 +44,7 @@ __device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, in
   mp = r / a.batches;
 }
 
-template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS>
+template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = kEpiPlain>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ GemmArgs args) {
@@ -76,7 +76,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
-      mbar_init(smem_u32(&tempty[i]), 2 * 128);
+      mbar_init(smem_u32(&tempty[i]), 2 * 4);  // one arrival per epilogue warp of each CTA
     }
     mbar_init(smem_u32(done), 1);
     fence_mbar_init();
@@ -214,13 +214,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     for (int tile = pair; tile < args.num_tiles; tile += npairs) {
       int batch, mp, nt;
       pair_decode_tile(args, tile, batch, mp, nt);
-      if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim)) break;
+      // warp-uniform: the lanes leave together (they share .sync.aligned ops)
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
       tc_fence_after();
       const int m = (2 * mp + static_cast<int>(rank)) * kBlockM + row;
       const int n0 = nt * BN;
       const bool row_ok = m < args.m_total;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * S::kAccCols;
-      const long long roff = static_cast<long long>(batch) * args.out_batch + static_cast<long long>(m) * args.out_ld;
+      const long long roff = row_ok ? epi_row_offset<EPI>(args, batch, m) : 0;
+      const long long soff = static_cast<long long>(m) * args.out_ld;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 16) {
         uint32_t r[16];
@@ -228,61 +230,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tmem_ld16(tbase + c, r);
         tmem_wait16(r);
         const int n = n0 + c;
-        if (!row_ok || n >= args.n_total) continue;
-        const bool full_chunk = n + 16 <= args.n_total;
-        if (OUT_F32) {
-          float* o = static_cast<float*>(args.out) + roff + n;
-          if (full_chunk) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              reinterpret_cast<float4*>(o)[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (n + j < args.n_total) o[j] = __uint_as_float(r[j]);
-          }
-        } else {
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-          if (HAS_BIAS) {
-            if (full_chunk) {
-              const uint4* bp = reinterpret_cast<const uint4*>(args.bias + n);
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                uint4 bb = __ldg(bp + hh);
-                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bb);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  float2 f = __bfloat1622float2(b2[j]);
-                  v[8 * hh + 2 * j] += f.x;
-                  v[8 * hh + 2 * j + 1] += f.y;
-                }
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (n + j < args.n_total) v[j] += __bfloat162float(args.bias[n + j]);
-            }
-          }
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) + roff + n;
-          if (full_chunk) {
-            uint4 pk[2];
-            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) p2[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-            reinterpret_cast<uint4*>(o)[0] = pk[0];
-            reinterpret_cast<uint4*>(o)[1] = pk[1];
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (n + j < args.n_total) o[j] = __float2bfloat16_rn(v[j]);
-          }
-        }
+        if (row_ok && n < args.n_total) epi_store16<OUT_F32, HAS_BIAS, EPI>(args, roff, soff, n, r);
       }
       tc_fence_before();
-      mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;

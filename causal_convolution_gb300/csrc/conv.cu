@@ -209,3 +209,59 @@ extern "C" cc_status cc_resample_phase_conv(const cc_bf16* x, const cc_bf16* pw,
   if (pair) return launch_tc_gemm_pair<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
   return launch_tc_gemm<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
 }
+
+extern "C" cc_status cc_resample_up2_fused(const cc_bf16* x, const cc_bf16* pw, const cc_bf16* bias,
+                                           const cc_bf16* skip, cc_bf16* out, int n, int d, int hl, int wl, int cin,
+                                           int cout, int hist, void* stream) {
+  const char* what = "resample_up2_fused";
+  cc_status st = check_ptrs(what, {x, pw, bias, skip, out});
+  if (st != CC_OK) return st;
+  if ((st = check_grid(what, n, d, hl, wl, hist)) != CC_OK) return st;
+  if (cin <= 0 || cout <= 0) return fail(CC_ERR_INVALID, "%s: channel counts must be positive", what);
+  if (cin % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C_in must be a multiple of 64 (got %d)", what, cin);
+  if (cout % 16 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C_out must be a multiple of 16 (got %d)", what, cout);
+  if ((long long)n * d * 4 * hl * wl > kMaxPositions * 4LL)
+    return fail(CC_ERR_UNSUPPORTED, "%s: too many positions", what);
+  DeviceInfo di;
+  if ((st = device_info(&di)) != CC_OK) return st;
+
+  const int lo_d = hist ? 0 : -2;
+  CUtensorMap ta, tb;
+  if ((st = encode_im2col_5d(&ta, x, n, d + hist, hl, wl, cin, -1, -1, lo_d, -1, -1, -2, kBlockM, kBlockK)) != CC_OK)
+    return st;
+  const long long m = (long long)n * d * hl * wl;
+  const bool pair = m > kBlockM;
+  if ((st = encode_tiled_2d(&tb, pw, cin, 48ull * cout, 2ull * cin, kBlockK, pair ? 128 : 256)) != CC_OK) return st;
+
+  GemmArgs a{};
+  a.m_total = static_cast<int>(m);
+  a.n_total = cout;
+  a.m_tiles = ceil_div(m, kBlockM);
+  a.n_tiles = ceil_div(cout, 256);
+  a.batches = 4;
+  a.num_tiles = a.m_tiles * a.n_tiles * 4;
+  a.taps = 12;
+  a.kb_per_tap = cin / kBlockK;
+  a.img_w = wl;
+  a.img_h = hl;
+  a.img_d = d;
+  a.lo_w = -1;
+  a.lo_h = -1;
+  a.lo_d = lo_d;
+  for (int ph = 0; ph < 4; ++ph) {
+    const int p = ph >> 1, q = ph & 1;
+    for (int kt = 0; kt < 3; ++kt)
+      for (int aa = 0; aa < 2; ++aa)
+        for (int bb = 0; bb < 2; ++bb) a.tap_off[ph * 12 + (kt * 2 + aa) * 2 + bb] = (q + bb) | ((p + aa) << 8) | (kt << 16);
+  }
+  a.b_rows_per_tap = cout;
+  a.b_rows_per_batch = 12 * cout;
+  a.out = out;
+  a.out_ld = cout;  // also the shortcut's row stride
+  a.out_batch = 0;
+  a.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
+  a.skip = reinterpret_cast<const __nv_bfloat16*>(skip);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pair) return launch_tc_gemm_pair<256, kAIm2col, false, false, true, kEpiResample>(ta, tb, a, di, s, what);
+  return launch_tc_gemm<256, kAIm2col, false, false, true, kEpiResample>(ta, tb, a, di, s, what);
+}

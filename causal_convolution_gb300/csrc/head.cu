@@ -12,8 +12,13 @@
 //    -- through three of four TMEM accumulators (4 x 128 columns), so an
 //    output is complete, and drained by the epilogue warps, as soon as its
 //    last (kt = 2) frame has been multiplied in.
-// Warp 0 streams A with TMA, warp 1 issues tcgen05.mma (M=128, N=112, K=16),
-// warps 2-5 drain accumulators to bf16 g. Every wait is bounded.
+//  - CTAs work in pairs (cta_group::2): a pair owns two neighbouring tiles,
+//    each CTA streams its own tile and keeps half of the weight's rows
+//    (56 of each tap's 112, 86 KB), so 8 A stages (128 KB) fit beside it and
+//    enough input is in flight to run at the copy bandwidth; one
+//    tcgen05.mma.cta_group::2 (M=256, N=112) from the even CTA covers both.
+// Warp 0 streams A with TMA, warp 1 of the even CTA issues the MMAs, warps 2-5
+// of both CTAs drain accumulators to bf16 g. Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -35,7 +40,8 @@ constexpr int kSmemBudget = 232448;
 struct HeadArgs {
   int plane;        // positions per frame (H*W)
   int plane_tiles;  // 128-position tiles per frame
-  int units;        // images x plane tiles
+  int pair_tiles;   // pairs of tiles per frame: ceil(plane_tiles / 2)
+  int units;        // images x pair_tiles
   int d_in;         // frames of x per image (D + hist)
   int d_out;        // output frames per image
   int hist;         // 0 or 2
@@ -46,12 +52,14 @@ struct HeadArgs {
 
 template <int CB>  // C_in / 64
 struct HeadShape {
-  static constexpr int kBBlock = kHeadN * kBlockK * 2;  // one tap x 64 channels: 14,336 B
+  static constexpr int kHalfN = kHeadN / 2;              // weight rows per CTA of the pair
+  static constexpr int kBBlock = kHalfN * kBlockK * 2;   // one tap x 64 channels, this CTA's half: 7168 B
   static constexpr int kBBytes = 3 * CB * kBBlock;
   static constexpr int kABytes = kBlockM * kBlockK * 2;
-  static constexpr int kAStagesFit = (kSmemBudget - 1024 - 256 - kBBytes) / kABytes;
-  static constexpr int kAStages = kAStagesFit > 8 ? 8 : kAStagesFit;
-  static constexpr int kSmemBytes = 1024 + kBBytes + kAStages * kABytes + 256;
+  static constexpr int kOutBytes = kBlockM * kHeadN * 2;  // one output tile staged for a bulk store: 28 KB
+  static constexpr int kAStagesFit = (kSmemBudget - 1024 - 256 - kBBytes - kOutBytes) / kABytes;
+  static constexpr int kAStages = kAStagesFit > 6 ? 6 : kAStagesFit;
+  static constexpr int kSmemBytes = 1024 + kBBytes + kAStages * kABytes + kOutBytes + 256;
   static_assert(kBBlock % 1024 == 0, "weight blocks must keep 1024-byte swizzle atoms aligned");
   static_assert(kAStages >= 2, "at least two A stages");
   static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
@@ -61,7 +69,7 @@ struct HeadShape {
 __device__ __forceinline__ int first_frame(int u, int hist) { return max(0, u + hist - 2); }
 
 template <int CB>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     head_temporal_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                          const __grid_constant__ HeadArgs a) {
   using S = HeadShape<CB>;
@@ -70,7 +78,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sB = smem;
   uint8_t* sA = smem + S::kBBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + AST * S::kABytes);
+  uint8_t* sOut = sA + AST * S::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + S::kOutBytes);
   uint64_t* afull = bars;
   uint64_t* aempty = bars + AST;
   uint64_t* bfull = bars + 2 * AST;
@@ -81,6 +90,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
   if (threadIdx.x == 0) {
     for (int s = 0; s < AST; ++s) {
       mbar_init(smem_u32(&afull[s]), 1);
@@ -89,7 +102,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(smem_u32(bfull), 1);
     for (int i = 0; i < kHeadSlots; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
-      mbar_init(smem_u32(&tempty[i]), 128);
+      mbar_init(smem_u32(&tempty[i]), 2 * 4);  // one arrival per epilogue warp of each CTA
     }
     mbar_init(smem_u32(done), 1);
     fence_mbar_init();
@@ -97,11 +110,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_map(&tmW);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kHeadSlots * kHeadAccCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), kHeadSlots * kHeadAccCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t tlim = a.timeout_ns;
@@ -109,26 +122,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer --
     if (lane == 0) {
-      const uint32_t bb = smem_u32(bfull);
-      mbar_arrive_expect_tx(bb, S::kBBytes);
+      // this CTA's half of the weight: rows rank*56 .. rank*56+55 of each tap
+      const uint32_t bb_local = smem_u32(bfull);
+      const uint32_t bb = mapa_shared(bb_local, 0);
+      if (leader) mbar_arrive_expect_tx(bb_local, 2 * S::kBBytes);
       for (int tap = 0; tap < 3; ++tap)
         for (int kb = 0; kb < CB; ++kb)
-          tma_load_2d(smem_u32(sB + (tap * CB + kb) * S::kBBlock), &tmW, bb, kb * kBlockK, tap * kHeadN);
+          tma_load_2d_pair(smem_u32(sB + (tap * CB + kb) * S::kBBlock), &tmW, bb, kb * kBlockK,
+                           tap * kHeadN + static_cast<int>(rank) * S::kHalfN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < a.units; unit += gridDim.x) {
-        const int img = unit / a.plane_tiles;
-        const int m0 = (unit - img * a.plane_tiles) * kBlockM;
+      for (int unit = pair; ok && unit < a.units; unit += npairs) {
+        const int img = unit / a.pair_tiles;
+        const int m0 = (2 * (unit - img * a.pair_tiles) + static_cast<int>(rank)) * kBlockM;
         for (int f = 0; ok && f < a.d_in; ++f) {
           for (int kb = 0; kb < CB; ++kb) {
             if (!mbar_wait(smem_u32(&aempty[stage]), phase ^ 1u, a.err, tlim)) {
               ok = false;
               break;
             }
-            const uint32_t fb = smem_u32(&afull[stage]);
-            mbar_arrive_expect_tx(fb, S::kABytes);
-            tma_load_3d(smem_u32(sA + stage * S::kABytes), &tmX, fb, kb * kBlockK, m0, img * a.d_in + f);
+            const uint32_t fb_local = smem_u32(&afull[stage]);
+            if (leader) mbar_arrive_expect_tx(fb_local, 2 * S::kABytes);
+            tma_load_3d_pair(smem_u32(sA + stage * S::kABytes), &tmX, mapa_shared(fb_local, 0), kb * kBlockK, m0,
+                             img * a.d_in + f);
             if (++stage == AST) {
               stage = 0;
               phase ^= 1u;
@@ -136,22 +153,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      if (!ok) {
-        for (int s = 0; s < AST; ++s)
-          (void)mbar_wait(smem_u32(&afull[s]), (s < stage) ? phase : (phase ^ 1u), a.err, 200000000ull);
+      if (leader) {
+        // copies of both CTAs complete on the even CTA's barriers
+        if (!ok)
+          for (int s = 0; s < AST; ++s)
+            (void)mbar_wait(smem_u32(&afull[s]), (s < stage) ? phase : (phase ^ 1u), a.err, 200000000ull);
+        (void)mbar_wait(bb_local, 0, a.err, 200000000ull);
       }
-      (void)mbar_wait(bb, 0, a.err, 200000000ull);  // the weight copies have landed before any exit
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer --
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kHeadN, false);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBlockM, kHeadN, false);
       bool ok = mbar_wait(smem_u32(bfull), 0, a.err, tlim);
       tc_fence_after();
       int stage = 0;
       uint32_t phase = 0;
       int q_base = 0;  // sequence number of this unit's output 0 among this CTA's outputs
-      for (int unit = blockIdx.x; ok && unit < a.units; unit += gridDim.x) {
+      for (int unit = pair; ok && unit < a.units; unit += npairs) {
         for (int f = 0; ok && f < a.d_in; ++f) {
           // Outputs this frame starts must have their accumulator slot drained.
           for (int kt = 0; kt < 3; ++kt) {
@@ -181,10 +200,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const uint32_t b_addr = smem_u32(sB + (kt * CB + kb) * S::kBBlock);
 #pragma unroll
               for (int k = 0; k < kBlockK / kUmmaK; ++k)
-                mma_bf16(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024), sdesc_sw128(b_addr + k * 32, 16, 1024), idesc,
-                         (first && k == 0) ? 0u : 1u);
+                mma_bf16_pair(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024), sdesc_sw128(b_addr + k * 32, 16, 1024),
+                              idesc, (first && k == 0) ? 0u : 1u);
             }
-            mma_commit(smem_u32(&aempty[stage]));
+            mma_commit_pair_both(smem_u32(&aempty[stage]));
             if (++stage == AST) {
               stage = 0;
               phase ^= 1u;
@@ -192,58 +211,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           if (!ok) break;
           const int u_done = f - a.hist;  // its kt = 2 frame was the last one
-          if (u_done >= 0 && u_done < a.d_out) mma_commit(smem_u32(&tfull[(q_base + u_done) & 3]));
+          if (u_done >= 0 && u_done < a.d_out) mma_commit_pair_both(smem_u32(&tfull[(q_base + u_done) & 3]));
         }
         q_base += a.d_out;
       }
-      mma_commit(smem_u32(done));
+      mma_commit_pair_both(smem_u32(done));
       (void)mbar_wait(smem_u32(done), 0, a.err, tlim);
     }
   } else {
     // -------------------------------------------------------- epilogue --
+    // Per output: all 112 columns of this thread's row come out of TMEM in
+    // one go, the slot is released at once, and the 128 x 112 bf16 tile --
+    // contiguous in g -- leaves through shared memory as one bulk copy.
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    const bool issuer = (warp == 2 && lane == 0);
+    uint8_t* my_row = sOut + row * (kHeadN * 2);
     int q = 0;
     bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < a.units; unit += gridDim.x) {
-      const int img = unit / a.plane_tiles;
-      const int m = (unit - img * a.plane_tiles) * kBlockM + row;
-      const bool row_ok = m < a.plane;
+    for (int unit = pair; ok && unit < a.units; unit += npairs) {
+      const int img = unit / a.pair_tiles;
+      const int m0 = (2 * (unit - img * a.pair_tiles) + static_cast<int>(rank)) * kBlockM;
+      const int rows = min(kBlockM, a.plane - m0);  // may be <= 0 for the odd CTA of the last pair
       for (int u = 0; u < a.d_out; ++u, ++q) {
         const int slot = q & 3;
-        if (!mbar_wait(smem_u32(&tfull[slot]), (q >> 2) & 1, a.err, tlim)) {
+        // uniform over the four epilogue warps: they leave together, since
+        // they share .sync.aligned TMEM loads and named barriers
+        if (!named_barrier_and(1, 128, mbar_wait(smem_u32(&tfull[slot]), (q >> 2) & 1, a.err, tlim))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * kHeadAccCols;
-        __nv_bfloat16* out = a.g + ((long long)(img * a.d_out + u) * a.plane + m) * kHeadN;
-#pragma unroll 1
-        for (int c = 0; c < kHeadN; c += 16) {
-          uint32_t r[16];
-          __syncwarp();
-          tmem_ld16(tbase + c, r);
-          tmem_wait16(r);
-          if (row_ok) {
-            uint4 pk[2];
-            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
+        uint32_t r[7][16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) p2[j] = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-            reinterpret_cast<uint4*>(out + c)[0] = pk[0];
-            reinterpret_cast<uint4*>(out + c)[1] = pk[1];
-          }
-        }
+        for (int c = 0; c < 7; ++c) tmem_ld16(tbase + c * 16, r[c]);
+#pragma unroll
+        for (int c = 0; c < 7; ++c) tmem_wait16(r[c]);
         tc_fence_before();
-        mbar_arrive(smem_u32(&tempty[slot]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[slot]), 0));
+        // the previous output's bulk store must have read the staging tile
+        if (issuer) bulk_wait_read_all();
+        named_barrier_sync(1, 128);
+#pragma unroll
+        for (int c = 0; c < 7; ++c) {
+          uint4 pk[2];
+          __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            p2[j] = __floats2bfloat162_rn(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1]));
+          reinterpret_cast<uint4*>(my_row + c * 32)[0] = pk[0];
+          reinterpret_cast<uint4*>(my_row + c * 32)[1] = pk[1];
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (issuer && rows > 0) {
+          bulk_store(a.g + ((long long)(img * a.d_out + u) * a.plane + m0) * kHeadN, smem_u32(sOut),
+                     static_cast<uint32_t>(rows) * kHeadN * 2);
+          bulk_commit();
+        }
       }
     }
+    if (issuer) bulk_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kHeadSlots * kHeadAccCols);
+    tmem_dealloc_pair(tmem_base, kHeadSlots * kHeadAccCols);
   }
 }
 
@@ -279,7 +317,7 @@ cc_status launch_head_temporal(const CUtensorMap& tx, const CUtensorMap& tw, Hea
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "head_temporal: shared-memory attribute: %s", cudaGetErrorString(e));
   a.err = di.err_word;
   a.timeout_ns = kWaitLimitNs;
-  kern<<<std::min(a.units, di.sm_count), kGemmThreads, S::kSmemBytes, stream>>>(tx, tw, a);
+  kern<<<2 * std::min(a.units, di.sm_count / 2), kGemmThreads, S::kSmemBytes, stream>>>(tx, tw, a);
   return launch_status("head_temporal");
 }
 
@@ -320,11 +358,13 @@ extern "C" cc_status cc_head_temporal(const cc_bf16* x, const cc_bf16* wp, cc_bf
   if ((st = encode_tiled_3d(&tx, x, cin, plane, (uint64_t)n * (d + hist), 2ull * cin, 2ull * cin * plane, kBlockK,
                             kBlockM)) != CC_OK)
     return st;
-  if ((st = encode_tiled_2d(&tw, wp, cin, 3ull * CC_HEAD_G_CH, 2ull * cin, kBlockK, CC_HEAD_G_CH)) != CC_OK) return st;
+  if ((st = encode_tiled_2d(&tw, wp, cin, 3ull * CC_HEAD_G_CH, 2ull * cin, kBlockK, CC_HEAD_G_CH / 2)) != CC_OK)
+    return st;
   HeadArgs a{};
   a.plane = static_cast<int>(plane);
   a.plane_tiles = ceil_div(plane, kBlockM);
-  a.units = n * a.plane_tiles;
+  a.pair_tiles = (a.plane_tiles + 1) / 2;
+  a.units = n * a.pair_tiles;
   a.d_in = d + hist;
   a.d_out = d;
   a.hist = hist;

@@ -124,6 +124,15 @@ cc_status cc_resample_up2(const cc_bf16* x, const cc_bf16* pw, const cc_bf16* bi
                           cc_bf16* out, int n, int d, int hl, int wl, int cin, int cout, int hist, void* ws,
                           size_t ws_bytes, void* stream);
 
+/* The whole resampler in ONE kernel, no workspace: the phase-convolution
+ * epilogue adds the bias and the shortcut to each accumulator row in fp32 and
+ * writes it, rounded once, straight to its interleaved high-resolution
+ * position (the interleave pass of [RES] done in registers, so the four phase
+ * tensors never reach memory). Same arguments and result as cc_resample_up2
+ * up to rounding (one bf16 rounding instead of two). */
+cc_status cc_resample_up2_fused(const cc_bf16* x, const cc_bf16* pw, const cc_bf16* bias, const cc_bf16* skip,
+                                cc_bf16* out, int n, int d, int hl, int wl, int cin, int cout, int hist, void* stream);
+
 /* ------------------------------------------------ per-frame attention [ATTN] */
 
 /* Row stride (elements) used for S (fp32) and P (bf16) inside the workspace. */

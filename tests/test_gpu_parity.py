@@ -389,3 +389,59 @@ def test_kernel_wait_timeout_is_reported_and_cleared():
     inp, _, y = run_conv(1, 1, 2, 3, 64, 16, 0)
     ref = oracle.causal_conv3d(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]))
     assert_parity(to_np(y), ref, "conv after a timeout")
+
+
+# ------------------------------------------------------ fused resampler --
+
+def run_resample_fused(x, w, b, skip, hist=0):
+    n, dd, hl, wl, cin = x.shape
+    d = dd - hist
+    cout = w.shape[0]
+    pw = prepare_resample(w)
+    out = empty(n, d, 2 * hl, 2 * wl, cout)
+    api.cc_resample_up2_fused(x, pw, b, skip, out, hist=hist)
+    api.cc_check_device()
+    return out
+
+
+def test_resample_fused_toy_config_full():
+    inp = inputs.make_config_inputs("toy_resampler", device=DEV)
+    out = run_resample_fused(inp["x"], inp["w"], inp["b"], inp["skip"])
+    ref = oracle.resample_up2(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]), to_np(inp["skip"]))
+    assert_parity(to_np(out), ref, "toy resampler, fused")
+
+
+@pytest.mark.parametrize("n,d,hl,wl,cin,cout,hist", [
+    (1, 3, 5, 7, 64, 128, 0),
+    (2, 2, 3, 4, 128, 64, 2),
+    (1, 2, 9, 13, 64, 272, 0),
+    (1, 1, 1, 1, 64, 16, 0),     # a single low-resolution pixel (single-CTA path)
+])
+def test_resample_fused_small(n, d, hl, wl, cin, cout, hist):
+    g = torch.Generator(device=DEV).manual_seed(22)
+    x = torch.randn((n, d + hist, hl, wl, cin), generator=g, device=DEV).to(BF16)
+    w = (torch.randn((cout, cin, 3, 3, 3), generator=g, device=DEV) / (27 * cin) ** 0.5).to(BF16)
+    b = (torch.randn((cout,), generator=g, device=DEV) * 0.1).to(BF16)
+    s = torch.randn((n, d, hl, wl, cout), generator=g, device=DEV).to(BF16)
+    out = run_resample_fused(x, w, b, s, hist)
+    xn = to_np(x)
+    ref = oracle.resample_up2(xn[:, hist:], to_np(w), to_np(b), to_np(s), history=xn[:, :2] if hist else None)
+    assert_parity(to_np(out), ref, f"fused resampler {n,d,hl,wl,cin,cout,hist}")
+
+
+def test_resample_fused_matches_two_pass():
+    inp = inputs.resample_inputs(1, 2, 6, 10, 128, seed=23, device=DEV)
+    _, two_pass, _ = run_resample(inp["x"], inp["w"], inp["b"], inp["skip"])
+    fused = run_resample_fused(inp["x"], inp["w"], inp["b"], inp["skip"])
+    # the two-pass path rounds the phases to bf16 once more; both meet the bar
+    assert_parity(to_np(fused), to_np(two_pass), "fused vs two-pass", rel_l2=4e-3)
+
+
+def test_resample_fused_config_sampled():
+    c = inputs.CONFIGS["resampler"]
+    inp = inputs.make_config_inputs("resampler", device=DEV)
+    out = run_resample_fused(inp["x"], inp["w"], inp["b"], inp["skip"])
+    pts = edge_points(c.n, c.d, 2 * c.h, 2 * c.w, 160, np.random.default_rng(5))
+    ref = oracle.resample_up2_at(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]), to_np(inp["skip"]), pts)
+    got = to_np(out)[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]]
+    assert_parity(got, ref, "fused resampler sampled")
