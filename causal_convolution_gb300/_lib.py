@@ -30,7 +30,8 @@ SIGNATURES = {
     "cc_resample_phase_conv": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "cc_resample_interleave": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "cc_resample_up2": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
-    "cc_resample_up2_fused": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "cc_resample_prepare_temporal": (_I, [_P, _P, _I, _I, _P]),
+    "cc_resample_up2_fused": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "cc_attn_ld": (_L, [_I]),
     "cc_attn_workspace_bytes": (_Z, [_I, _I]),
     "cc_attn_scores": (_I, [_P, _P, _P, _I, _I, _I, _L, _L, _L, _P]),

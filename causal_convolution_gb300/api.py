@@ -18,7 +18,7 @@ __all__ = [
     "CCError", "cc_version", "cc_check_device",
     "cc_conv3d_prepare", "cc_conv3d_causal",
     "cc_resample_prepare", "cc_resample_workspace_bytes", "cc_resample_phase_conv", "cc_resample_interleave",
-    "cc_resample_up2", "cc_resample_up2_fused",
+    "cc_resample_up2", "cc_resample_up2_fused", "cc_resample_prepare_temporal",
     "cc_attn_ld", "cc_attn_workspace_bytes", "cc_attn_scores", "cc_attn_softmax", "cc_attn_pv", "cc_attn_frame",
     "cc_head_prepare", "cc_head_workspace_bytes", "cc_head_temporal", "cc_head_stencil", "cc_head_out",
     "cc_head_out_noalloc", "HEAD_NOALLOC_SCRATCH_BYTES",
@@ -143,17 +143,27 @@ def cc_resample_up2(x, pw, bias, skip, out, ws, hist: int = 0, stream=None) -> N
                                        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
 
 
-def cc_resample_up2_fused(x, pw, bias, skip, out, hist: int = 0, stream=None) -> None:
-    n, d, h2, w2, cout = out.shape
+def cc_resample_prepare_temporal(w, pw, stream=None) -> None:
+    cout, cin = w.shape[:2]
+    if tuple(w.shape) != (cout, cin, 3, 3, 3) or pw.numel() != 64 * cout * cin:
+        raise ValueError("resample_prepare_temporal: w must be [Cout,Cin,3,3,3] and pw hold 64*Cout*Cin elements")
+    _check(_lib.load().cc_resample_prepare_temporal(_ptr(w, name="w"), _ptr(pw, name="pw"), cout, cin,
+                                                    _stream(stream)))
+
+
+def cc_resample_up2_fused(x, pw, bias, skip, out, hist: int = 0, temporal: bool = False, stream=None) -> None:
+    n, d2, h2, w2, cout = out.shape
     hl, wl = h2 // 2, w2 // 2
+    d = d2 // 2 if temporal else d2
     cin = x.shape[-1]
-    if h2 != 2 * hl or w2 != 2 * wl or tuple(x.shape) != (n, d + hist, hl, wl, cin):
-        raise ValueError("resample_up2_fused: out must be [N,D,2HL,2WL,Cout] of x [N,D+hist,HL,WL,Cin]")
-    if tuple(skip.shape) != (n, d, hl, wl, cout) or bias.numel() != cout or pw.numel() != 48 * cout * cin:
+    if h2 != 2 * hl or w2 != 2 * wl or (temporal and d2 != 2 * d) or tuple(x.shape) != (n, d + hist, hl, wl, cin):
+        raise ValueError("resample_up2_fused: out must be [N,(2)D,2HL,2WL,Cout] of x [N,D+hist,HL,WL,Cin]")
+    taps = 64 if temporal else 48
+    if tuple(skip.shape) != (n, d, hl, wl, cout) or bias.numel() != cout or pw.numel() != taps * cout * cin:
         raise ValueError("resample_up2_fused: skip, bias or pw shape mismatch")
     _check(_lib.load().cc_resample_up2_fused(_ptr(x, name="x"), _ptr(pw, name="pw"), _ptr(bias, name="bias"),
                                              _ptr(skip, name="skip"), _ptr(out, name="out"), n, d, hl, wl, cin, cout,
-                                             hist, _stream(stream)))
+                                             hist, 1 if temporal else 0, _stream(stream)))
 
 
 # ------------------------------------------------------ per-frame attention --

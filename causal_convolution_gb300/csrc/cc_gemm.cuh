@@ -58,6 +58,7 @@ struct GemmArgs {
   long long out_batch;   // elements between batches
   const __nv_bfloat16* bias;  // per column, or nullptr
   const __nv_bfloat16* skip;  // resampler epilogue: shortcut rows (row m at m * out_ld)
+  int epi_tscale;             // resampler epilogue: 2 when the output is also x2 in time
   unsigned int* err;
   unsigned long long timeout_ns;
 };
@@ -92,9 +93,10 @@ __device__ __forceinline__ void gemm_decode_tile(const GemmArgs& a, int tile, in
 
 // Epilogue modes. Plain: row m of batch b goes to out + b*out_batch + m*out_ld.
 // Resample: the accumulator rows are low-resolution positions (frame f, row i,
-// column j) of output parity batch = 2p + q; the row is written, with the bias
-// and the shortcut row m added, to high-resolution position (f, 2i+p, 2j+q) of
-// out [frames, 2*img_h, 2*img_w, out_ld] -- the interleave done in registers.
+// column j) of output parity batch = 4s + 2p + q; the row is written, with the
+// bias and the shortcut row m added, to high-resolution position
+// (f*epi_tscale + s, 2i+p, 2j+q) of out [frames, 2*img_h, 2*img_w, out_ld] --
+// the interleave done in registers (s = 0 unless the output is x2 in time).
 enum EpiMode : int { kEpiPlain = 0, kEpiResample = 1 };
 
 template <int EPI>
@@ -104,8 +106,9 @@ __device__ __forceinline__ long long epi_row_offset(const GemmArgs& a, int batch
     const int r = m / a.img_w;
     const int i = r % a.img_h;
     const long long f = r / a.img_h;
-    const int p = batch >> 1, q = batch & 1;
-    return ((f * (2 * a.img_h) + 2 * i + p) * (2LL * a.img_w) + 2 * j + q) * a.out_ld;
+    const int q = batch & 1, p = (batch >> 1) & 1, s = batch >> 2;
+    const long long fo = a.epi_tscale == 2 ? 2 * f + s : f;
+    return ((fo * (2 * a.img_h) + 2 * i + p) * (2LL * a.img_w) + 2 * j + q) * a.out_ld;
   }
   return static_cast<long long>(batch) * a.out_batch + static_cast<long long>(m) * a.out_ld;
 }

@@ -124,14 +124,29 @@ cc_status cc_resample_up2(const cc_bf16* x, const cc_bf16* pw, const cc_bf16* bi
                           cc_bf16* out, int n, int d, int hl, int wl, int cin, int cout, int hist, void* ws,
                           size_t ws_bytes, void* stream);
 
+/* Temporal variant's pre-summed kernels ([RES]: for up_blocks 0 and 1 the
+ * phase kernels and the shortcut are nearest-x2 in time as well). Output
+ * frame 2t+s, row 2i+p, column 2j+q; phase tap (a, b, c) reads low-resolution
+ * frame t-1+a, row i+p-1+b, column j+q-1+c. Causal tap kt of up-sampled frame
+ * 2t+s lands on frame t-1+a for kt in {0,1} | {2} (s=0) or {0} | {1,2} (s=1);
+ * rows/columns as in cc_resample_prepare. Sums in fp32, rounded once:
+ * pw[(4s+2p+q)][(a*2+b)*2+c][co][ci]; 64*C_out*C_in elements. */
+cc_status cc_resample_prepare_temporal(const cc_bf16* w, cc_bf16* pw, int cout, int cin, void* stream);
+
 /* The whole resampler in ONE kernel, no workspace: the phase-convolution
  * epilogue adds the bias and the shortcut to each accumulator row in fp32 and
  * writes it, rounded once, straight to its interleaved high-resolution
- * position (the interleave pass of [RES] done in registers, so the four phase
- * tensors never reach memory). Same arguments and result as cc_resample_up2
- * up to rounding (one bf16 rounding instead of two). */
+ * position (the interleave pass of [RES] done in registers, so the phase
+ * tensors never reach memory). temporal = 0: pw from cc_resample_prepare, out
+ * [N, D, 2HL, 2WL, C_out], same result as cc_resample_up2 up to rounding (one
+ * bf16 rounding instead of two). temporal = 1: pw from
+ * cc_resample_prepare_temporal, nearest x2 in time as well -- out
+ * [N, 2D, 2HL, 2WL, C_out], shortcut duplicated in time too; with hist = 2
+ * only the last history frame matters (it fills both up-sampled frames
+ * before frame 0). skip: [N, D, HL, WL, C_out]. */
 cc_status cc_resample_up2_fused(const cc_bf16* x, const cc_bf16* pw, const cc_bf16* bias, const cc_bf16* skip,
-                                cc_bf16* out, int n, int d, int hl, int wl, int cin, int cout, int hist, void* stream);
+                                cc_bf16* out, int n, int d, int hl, int wl, int cin, int cout, int hist, int temporal,
+                                void* stream);
 
 /* ------------------------------------------------ per-frame attention [ATTN] */
 

@@ -52,6 +52,8 @@ __all__ = [
     "resample_phase_conv",
     "resample_interleave",
     "resample_up2_four_phase",
+    "resample_phase_kernels_temporal",
+    "resample_up2_temporal_eight_phase",
     "attn_probs",
     "attn_frame",
     "attn_frame_rows",
@@ -138,22 +140,33 @@ def causal_conv3d_at(x, w, b, points, history=None) -> np.ndarray:
     return out
 
 
-def nearest_up2(x) -> np.ndarray:
-    """Nearest-neighbour x2 in space: u[n,t,y,x,c] = x[n,t,y//2,x//2,c]."""
+def nearest_up2(x, temporal=False) -> np.ndarray:
+    """Nearest-neighbour x2 in space: u[n,t,y,x,c] = x[n,t,y//2,x//2,c]; with
+    ``temporal`` also x2 in time: u[n,T,y,x,c] = x[n,T//2,y//2,x//2,c]."""
     x = _f64(x)
-    return np.repeat(np.repeat(x, 2, axis=2), 2, axis=3)
+    u = np.repeat(np.repeat(x, 2, axis=2), 2, axis=3)
+    return np.repeat(u, 2, axis=1) if temporal else u
 
 
-def resample_up2(x, w, b, skip, history=None) -> np.ndarray:
-    """Spatial resampler, direct form: nearest x2 in space, the causal 3x3x3
-    convolution with bias, then the nearest-duplicated shortcut added."""
-    hist_up = None if history is None else nearest_up2(history)
-    return causal_conv3d(nearest_up2(x), w, b, hist_up) + nearest_up2(skip)
+def resample_up2(x, w, b, skip, history=None, temporal=False) -> np.ndarray:
+    """Resampler, direct form: nearest x2 in space (and in time when
+    ``temporal``, the resample.h variant of up_blocks 0 and 1), the causal
+    3x3x3 convolution with bias, then the equally duplicated shortcut added.
+    In the temporal variant the up-sampled history is the last history frame
+    twice (nearest x2 of frames -2, -1 keeps only frame -1 next to frame 0)."""
+    if history is None:
+        hist_up = None
+    elif temporal:
+        hist_up = nearest_up2(np.asarray(history)[:, 1:2], temporal=True)
+    else:
+        hist_up = nearest_up2(history)
+    return causal_conv3d(nearest_up2(x, temporal), w, b, hist_up) + nearest_up2(skip, temporal)
 
 
-def resample_up2_at(x, w, b, skip, points, history=None) -> np.ndarray:
+def resample_up2_at(x, w, b, skip, points, history=None, temporal=False) -> np.ndarray:
     """The direct resampler at high-resolution ``points`` [P,4] of
-    (n, t, y, x); the up-sampled tensor is indexed, never materialised."""
+    (n, t, y, x); the up-sampled tensor is indexed, never materialised. With
+    ``temporal`` the output frame T reads low-resolution frame T // 2."""
     x = np.asarray(x)  # gathered windows are widened to float64 below
     w = _f64(w)
     pts = np.asarray(points, dtype=np.int64).reshape(-1, 4)
@@ -165,7 +178,8 @@ def resample_up2_at(x, w, b, skip, points, history=None) -> np.ndarray:
     for kt in range(3):
         for kh in range(3):
             for kw in range(3):
-                tt = pts[:, 1] + kt - 2
+                tu = pts[:, 1] + kt - 2  # frame of the (time-)up-sampled input
+                tt = np.floor_divide(tu, 2) if temporal else tu
                 yy = pts[:, 2] + kh - 1
                 xx = pts[:, 3] + kw - 1
                 inside = (yy >= 0) & (yy < hh_max) & (xx >= 0) & (xx < ww_max)
@@ -177,7 +191,8 @@ def resample_up2_at(x, w, b, skip, points, history=None) -> np.ndarray:
                     win[old] = hist[pts[old, 0], tt[old] + 2, yy[old] // 2, xx[old] // 2, :]
                 out += win @ w[:, :, kt, kh, kw].T
     s = np.asarray(skip)
-    out += s[pts[:, 0], pts[:, 1], pts[:, 2] // 2, pts[:, 3] // 2, :].astype(np.float64)
+    ts = pts[:, 1] // 2 if temporal else pts[:, 1]
+    out += s[pts[:, 0], ts, pts[:, 2] // 2, pts[:, 3] // 2, :].astype(np.float64)
     return out
 
 
@@ -236,6 +251,58 @@ def resample_interleave(phases, b, skip) -> np.ndarray:
     for p in range(2):
         for q in range(2):
             out[:, :, p::2, q::2, :] = ph[2 * p + q] + _f64(b) + _f64(skip)
+    return out
+
+
+# Taps kt of up-sampled output frame 2t+s that land on low-resolution frame
+# t-1+a (causal: tap kt reads up-sampled frame 2t+s+kt-2).
+_PHASE_FRAMES = {(0, 0): (0, 1), (0, 1): (2,), (1, 0): (0,), (1, 1): (1, 2)}
+
+
+def resample_phase_kernels_temporal(w) -> np.ndarray:
+    """Eight per-phase 2x2x2 kernels of the temporal variant: output frame
+    2t+s, row 2i+p, column 2j+q; phase tap (a, bb, cc) reads low-resolution
+    frame t-1+a, row i+p-1+bb, column j+q-1+cc. Causal tap kt of up-sampled
+    frame 2t+s reads up-sampled frame 2t+s+kt-2, i.e. low-resolution frames
+    t-1, t-1, t (s=0) or t-1, t, t (s=1): the grouping of rows with the parity
+    flipped. Returns pk[4s+2p+q, co, ci, a, bb, cc]."""
+    w = _f64(w)
+    cout, cin = w.shape[:2]
+    pk = np.zeros((8, cout, cin, 2, 2, 2), dtype=np.float64)
+    for s_ in range(2):
+        for p in range(2):
+            for q in range(2):
+                for a in range(2):
+                    for bb in range(2):
+                        for cc in range(2):
+                            for kt in _PHASE_FRAMES[(s_, a)]:
+                                for kh in _PHASE_ROWS[(p, bb)]:
+                                    for kw in _PHASE_ROWS[(q, cc)]:
+                                        pk[4 * s_ + 2 * p + q, :, :, a, bb, cc] += w[:, :, kt, kh, kw]
+    return pk
+
+
+def resample_up2_temporal_eight_phase(x, w, b, skip, history=None) -> np.ndarray:
+    """The temporal resampler through its eight-phase form, kept to check the
+    decomposition against the direct form (nearest x2 in time and space, then
+    the conv)."""
+    x = _f64(x)
+    n, d, hl, wl, cin = x.shape
+    pk = resample_phase_kernels_temporal(w)
+    cout = pk.shape[1]
+    xp = _pad_causal(x, history)  # frame t of x at index t + 2
+    out = np.zeros((n, 2 * d, 2 * hl, 2 * wl, cout), dtype=np.float64)
+    sk = _f64(skip)
+    for s_ in range(2):
+        for p in range(2):
+            for q in range(2):
+                ph = np.zeros((n, d, hl, wl, cout), dtype=np.float64)
+                for a in range(2):
+                    for bb in range(2):
+                        for cc in range(2):
+                            t0, r0, c0 = 1 + a, p + bb, q + cc  # frame t-1+a sits at index t+1+a
+                            ph += xp[:, t0:t0 + d, r0:r0 + hl, c0:c0 + wl, :] @ pk[4 * s_ + 2 * p + q, :, :, a, bb, cc].T
+                out[:, s_::2, p::2, q::2, :] = ph + _f64(b) + sk
     return out
 
 

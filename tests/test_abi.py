@@ -72,6 +72,7 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert lib.cc_conv3d_causal(p, p, None, p, 1, 1, 1, 1, 48, 64, 0, None) == 2  # C_in % 64
     assert b"multiple of 64" in lib.cc_last_error()
     assert lib.cc_resample_interleave(p, p, p, p, 1, 1, 1, 1, 12, None) == 2  # C % 8
+    assert lib.cc_resample_up2_fused(p, p, p, p, p, 1, 1, 1, 1, 64, 64, 0, 2, None) == 1  # temporal flag
     assert lib.cc_attn_softmax(p, p, 1, 16, 16, 16, ctypes.c_float(-1.0), None) == 1  # scale > 0
     assert lib.cc_attn_frame(p, p, p, p, 1, 16, 64, 64, 64, 64, 64, ctypes.c_float(0.125), p, 16, None) == 1
     assert b"workspace" in lib.cc_last_error()

@@ -445,3 +445,109 @@ def test_resample_fused_config_sampled():
     ref = oracle.resample_up2_at(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]), to_np(inp["skip"]), pts)
     got = to_np(out)[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]]
     assert_parity(got, ref, "fused resampler sampled")
+
+
+# --------------------------------------------- temporal resampler (x2 in time) --
+
+def test_resample_prepare_temporal_matches_oracle():
+    inp = inputs.resample_inputs(1, 1, 1, 1, 64, seed=24, device=DEV)
+    pw = empty(64 * 64 * 64)
+    api.cc_resample_prepare_temporal(inp["w"], pw)
+    pk = oracle.resample_phase_kernels_temporal(to_np(inp["w"]))  # [8, co, ci, a, b, c]
+    ref = pk.transpose(0, 3, 4, 5, 1, 2).reshape(-1)               # [phase][(a*2+b)*2+c][co][ci]
+    np.testing.assert_allclose(to_np(pw).astype(np.float64), ref, rtol=2.0 ** -8, atol=1e-30)
+
+
+def run_resample_temporal(x, w, b, skip, hist=0):
+    n, dd, hl, wl, cin = x.shape
+    d = dd - hist
+    cout = w.shape[0]
+    pw = empty(64 * cout * cin)
+    api.cc_resample_prepare_temporal(w, pw)
+    out = empty(n, 2 * d, 2 * hl, 2 * wl, cout)
+    api.cc_resample_up2_fused(x, pw, b, skip, out, hist=hist, temporal=True)
+    api.cc_check_device()
+    return out
+
+
+@pytest.mark.parametrize("n,d,hl,wl,cin,cout,hist", [
+    (1, 2, 8, 12, 64, 64, 0),
+    (1, 3, 5, 7, 64, 128, 2),
+    (2, 2, 3, 4, 128, 64, 0),
+    (1, 1, 1, 1, 64, 16, 2),
+])
+def test_resample_temporal_small(n, d, hl, wl, cin, cout, hist):
+    g = torch.Generator(device=DEV).manual_seed(25)
+    x = torch.randn((n, d + hist, hl, wl, cin), generator=g, device=DEV).to(BF16)
+    w = (torch.randn((cout, cin, 3, 3, 3), generator=g, device=DEV) / (27 * cin) ** 0.5).to(BF16)
+    b = (torch.randn((cout,), generator=g, device=DEV) * 0.1).to(BF16)
+    s = torch.randn((n, d, hl, wl, cout), generator=g, device=DEV).to(BF16)
+    out = run_resample_temporal(x, w, b, s, hist)
+    xn = to_np(x)
+    ref = oracle.resample_up2(xn[:, hist:], to_np(w), to_np(b), to_np(s), history=xn[:, :2] if hist else None,
+                              temporal=True)
+    assert out.shape == (n, 2 * d, 2 * hl, 2 * wl, cout)
+    assert_parity(to_np(out), ref, f"temporal resampler {n,d,hl,wl,cin,cout,hist}")
+
+
+def test_resample_temporal_sampled_large():
+    # an up-block-sized case: 512 channels, 4 latent frames at 44x78 -> 8 x 88x156
+    inp = inputs.resample_inputs(1, 4, 44, 78, 512, seed=26, device=DEV)
+    out = run_resample_temporal(inp["x"], inp["w"], inp["b"], inp["skip"])
+    pts = edge_points(1, 8, 88, 156, 120, np.random.default_rng(6))
+    ref = oracle.resample_up2_at(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]), to_np(inp["skip"]), pts,
+                                 temporal=True)
+    got = to_np(out)[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]]
+    assert_parity(got, ref, "temporal resampler sampled")
+
+
+# ------------------------------------------ chunked streaming with history --
+# A long video is decoded in chunks; each chunk after the first carries the
+# previous chunk's last two input frames as history (hist = 2). The result
+# must equal one call over all frames, bit for bit (same sums in the same order).
+
+def test_conv_chunked_streaming_equals_one_call():
+    n, d, h, w, c = 1, 8, 6, 10, 128
+    inp = inputs.conv_inputs(n, d, h, w, c, c, seed=27, device=DEV)
+    wp = empty(27 * c * c)
+    api.cc_conv3d_prepare(inp["w"], wp)
+    full = empty(n, d, h, w, c)
+    api.cc_conv3d_causal(inp["x"], wp, inp["b"], full)
+    y0, y1 = empty(n, 4, h, w, c), empty(n, 4, h, w, c)
+    api.cc_conv3d_causal(inp["x"][:, :4].contiguous(), wp, inp["b"], y0, hist=0)
+    api.cc_conv3d_causal(inp["x"][:, 2:].contiguous(), wp, inp["b"], y1, hist=2)
+    api.cc_check_device()
+    assert torch.equal(torch.cat([y0, y1], 1), full)
+
+
+def test_head_chunked_streaming_equals_one_call():
+    n, d, h, w, c = 1, 8, 8, 20, 64
+    inp = inputs.head_inputs(n, d, h, w, c, seed=28, device=DEV)
+    wp = empty(3 * api.HEAD_G_CH * c)
+    api.cc_head_prepare(inp["w"], wp)
+    ws = torch.empty(api.cc_head_workspace_bytes(n, d, h, w), dtype=torch.uint8, device=DEV)
+    full = empty(n, d, h, w, 12)
+    api.cc_head_out(inp["x"], wp, inp["b"], full, ws)
+    y0, y1 = empty(n, 4, h, w, 12), empty(n, 4, h, w, 12)
+    api.cc_head_out(inp["x"][:, :4].contiguous(), wp, inp["b"], y0, ws, hist=0)
+    api.cc_head_out(inp["x"][:, 2:].contiguous(), wp, inp["b"], y1, ws, hist=2)
+    api.cc_check_device()
+    assert torch.equal(torch.cat([y0, y1], 1), full)
+
+
+@pytest.mark.parametrize("temporal", [False, True])
+def test_resample_chunked_streaming_equals_one_call(temporal):
+    n, d, hl, wl, c = 1, 8, 6, 9, 64
+    inp = inputs.resample_inputs(n, d, hl, wl, c, seed=29, device=DEV)
+    pw = empty((64 if temporal else 48) * c * c)
+    (api.cc_resample_prepare_temporal if temporal else api.cc_resample_prepare)(inp["w"], pw)
+    ft = 2 if temporal else 1
+    full = empty(n, ft * d, 2 * hl, 2 * wl, c)
+    api.cc_resample_up2_fused(inp["x"], pw, inp["b"], inp["skip"], full, temporal=temporal)
+    y0, y1 = empty(n, ft * 4, 2 * hl, 2 * wl, c), empty(n, ft * 4, 2 * hl, 2 * wl, c)
+    api.cc_resample_up2_fused(inp["x"][:, :4].contiguous(), pw, inp["b"], inp["skip"][:, :4].contiguous(), y0,
+                              hist=0, temporal=temporal)
+    api.cc_resample_up2_fused(inp["x"][:, 2:].contiguous(), pw, inp["b"], inp["skip"][:, 4:].contiguous(), y1,
+                              hist=2, temporal=temporal)
+    api.cc_check_device()
+    assert torch.equal(torch.cat([y0, y1], 1), full)

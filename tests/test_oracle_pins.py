@@ -330,3 +330,54 @@ def test_interleave_places_each_phase_on_its_parity():
     # output row 2i+1, column 2j is phase 2*1+0 = 2
     np.testing.assert_array_equal(out[0, 1, 2 * 2 + 1, 2 * 3, :], ph[2, 0, 1, 2, 3] + b + s[0, 1, 2, 3])
     np.testing.assert_array_equal(out[0, 0, 0, 1, :], ph[1, 0, 0, 0, 0] + b + s[0, 0, 0, 0])
+
+
+# ------------------------------------------------- temporal resampler ----
+
+def torch_resample_temporal(x, w, b, s):
+    """Library routines: nearest interpolate x2 in (t, h, w), torch conv3d, shortcut likewise."""
+    up = lambda a: F.interpolate(torch.from_numpy(a).permute(0, 4, 1, 2, 3), scale_factor=(2, 2, 2), mode="nearest")
+    y = F.conv3d(F.pad(up(x), (1, 1, 1, 1, 2, 0)), torch.from_numpy(w), torch.from_numpy(b)) + up(s)
+    return y.permute(0, 2, 3, 4, 1).numpy()
+
+
+def test_resample_temporal_direct_matches_torch():
+    x, s = rnd(1, 3, 3, 4, 4), rnd(1, 3, 3, 4, 4)
+    w, b = rnd(4, 4, 3, 3, 3), rnd(4)
+    got = oracle.resample_up2(x, w, b, s, temporal=True)
+    assert got.shape == (1, 6, 6, 8, 4)
+    np.testing.assert_allclose(got, torch_resample_temporal(x, w, b, s), atol=1e-11)
+
+
+def test_resample_temporal_eight_phase_matches_direct():
+    x, s = rnd(1, 3, 4, 5, 8), rnd(1, 3, 4, 5, 6)
+    w, b = rnd(6, 8, 3, 3, 3), rnd(6)
+    hist = rnd(1, 2, 4, 5, 8)
+    for hh in (None, hist):
+        np.testing.assert_allclose(oracle.resample_up2_temporal_eight_phase(x, w, b, s, history=hh),
+                                   oracle.resample_up2(x, w, b, s, history=hh, temporal=True), rtol=0, atol=1e-12)
+
+
+def test_resample_temporal_history_uses_last_frame_only():
+    # nearest x2 in time puts low-resolution frame -1 at both up-sampled frames
+    # -2 and -1, so history frame -2 cannot matter
+    x, s = rnd(1, 2, 3, 3, 4), rnd(1, 2, 3, 3, 4)
+    w, b = rnd(4, 4, 3, 3, 3), rnd(4)
+    h1, h2 = rnd(1, 2, 3, 3, 4), rnd(1, 2, 3, 3, 4)
+    h2[:, 1] = h1[:, 1]
+    np.testing.assert_array_equal(oracle.resample_up2(x, w, b, s, history=h1, temporal=True),
+                                  oracle.resample_up2(x, w, b, s, history=h2, temporal=True))
+    full = oracle.resample_up2(np.concatenate([h1[:, 1:], x], 1), w, b, np.concatenate([s[:, :1], s], 1),
+                               temporal=True)
+    np.testing.assert_allclose(oracle.resample_up2(x, w, b, s, history=h1, temporal=True), full[:, 2:], atol=1e-12)
+
+
+def test_resample_temporal_sampled_matches_full():
+    x, s = rnd(1, 2, 3, 4, 3), rnd(1, 2, 3, 4, 3)
+    w, b = rnd(3, 3, 3, 3, 3), rnd(3)
+    hist = rnd(1, 2, 3, 4, 3)
+    pts = np.array(list(itertools.product(range(1), range(4), range(6), range(8))))
+    for hh in (None, hist):
+        full = oracle.resample_up2(x, w, b, s, history=hh, temporal=True)
+        at = oracle.resample_up2_at(x, w, b, s, pts, history=hh, temporal=True)
+        np.testing.assert_allclose(at, full[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]], atol=1e-12)
