@@ -294,6 +294,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       const int kblocks = args.taps * args.kb_per_tap;
+      // 8-row groups are 1024 bytes apart; MN-major 64-column blocks 8192 bytes
+      const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, 1024);
+      const uint64_t b_desc0 = B_MN ? sdesc_sw128(smem_u32(sB), 8192, 1024) : sdesc_sw128(smem_u32(sB), 16, 1024);
       for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
         if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, args.err, tlim)) {
           ok = false;
@@ -307,18 +310,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * S::kABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * S::kBBytes);
+          // stage and K offsets only move the descriptors' start-address field
+          // (16-byte units): K-major, the next 16 elements are 32 bytes on
+          // inside the 128-byte swizzle row; MN-major B (values), 16 keys are
+          // two 8-row groups of 128 bytes = 2048 bytes on.
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage) * (S::kABytes >> 4);
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (S::kBBytes >> 4);
 #pragma unroll
-          for (int k = 0; k < kBlockK / kUmmaK; ++k) {
-            // K-major: the next 16 elements are 32 bytes further inside the
-            // 128-byte swizzle row; 8-row groups are 1024 bytes apart.
-            const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
-            // MN-major B (values): 16 keys = 2 groups of 8 rows of 128 bytes;
-            // 64-column blocks are 8192 bytes apart.
-            const uint64_t bd = B_MN ? sdesc_sw128(b_addr + k * 2048, 8192, 1024) : sdesc_sw128(b_addr + k * 32, 16, 1024);
-            mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < kBlockK / kUmmaK; ++k)
+            mma_bf16(d_tmem, ad + 2 * k, bd + (B_MN ? 128 : 2) * k, idesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit(smem_u32(&empty[stage]));
           if (++stage == STAGES) {
             stage = 0;

@@ -165,6 +165,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------ MMA issuer --
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = idesc_bf16_f32(2 * kBlockM, kHeadN, false);
+      // descriptors of A stage 0 and weight block 0; the others differ only in
+      // the start-address field (all blocks are 1024-byte aligned)
+      const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, 1024);
+      const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), 16, 1024);
       bool ok = mbar_wait(smem_u32(bfull), 0, a.err, tlim);
       tc_fence_after();
       int stage = 0;
@@ -184,24 +188,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
           if (!ok) break;
           tc_fence_after();
+          // per frame: which of the three taps feed a live output, into which
+          // accumulator, and whether this frame starts that output
+          uint32_t d_col[3];
+          bool live[3], starts[3];
+#pragma unroll
+          for (int kt = 0; kt < 3; ++kt) {
+            const int u = f - a.hist + 2 - kt;
+            live[kt] = u >= 0 && u < a.d_out;
+            starts[kt] = live[kt] && f == first_frame(u, a.hist);
+            d_col[kt] = tmem_base + ((q_base + u) & 3) * kHeadAccCols;
+          }
           for (int kb = 0; kb < CB; ++kb) {
             if (!mbar_wait(smem_u32(&afull[stage]), phase, a.err, tlim)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(sA + stage * S::kABytes);
+            // K advances by 16 bf16 = 32 bytes = 2 in the descriptor's address field
+            const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage) * (S::kABytes >> 4);
 #pragma unroll
             for (int kt = 0; kt < 3; ++kt) {
-              const int u = f - a.hist + 2 - kt;
-              if (u < 0 || u >= a.d_out) continue;
-              const uint32_t d_tmem = tmem_base + ((q_base + u) & 3) * kHeadAccCols;
-              const bool first = (kb == 0) && (f == first_frame(u, a.hist));
-              const uint32_t b_addr = smem_u32(sB + (kt * CB + kb) * S::kBBlock);
+              if (!live[kt]) continue;
+              const uint64_t bd = b_desc0 + static_cast<uint64_t>((kt * CB + kb) * (S::kBBlock >> 4));
+              const uint32_t acc0 = (starts[kt] && kb == 0) ? 0u : 1u;
 #pragma unroll
               for (int k = 0; k < kBlockK / kUmmaK; ++k)
-                mma_bf16_pair(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024), sdesc_sw128(b_addr + k * 32, 16, 1024),
-                              idesc, (first && k == 0) ? 0u : 1u);
+                mma_bf16_pair(d_col[kt], ad + 2 * k, bd + 2 * k, idesc, k == 0 ? acc0 : 1u);
             }
             mma_commit_pair_both(smem_u32(&aempty[stage]));
             if (++stage == AST) {
