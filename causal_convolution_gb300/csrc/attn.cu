@@ -170,7 +170,13 @@ extern "C" cc_status cc_attn_scores(const cc_bf16* q, const cc_bf16* k, float* s
   a.out_ld = ld_s;
   a.out_batch = (long long)hw * ld_s;
   cudaStream_t s_ = static_cast<cudaStream_t>(stream);
-  if (pair) return launch_tc_gemm_pair<256, kATiled3d, false, true, false>(ta, tb, a, di, s_, what);
+  if (pair) {
+    // S leaves through TMA tensor stores of 32-column x 128-row fp32 boxes
+    CUtensorMap tc;
+    if ((st = encode_tiled_3d_f32_sw128(&tc, s, hw, hw, t, 4ull * ld_s, 4ull * ld_s * hw, 32, kBlockM)) != CC_OK)
+      return st;
+    return launch_tc_gemm_pair<256, kATiled3d, false, true, false, kEpiStoreF32>(ta, tb, a, di, s_, what, &tc);
+  }
   return launch_tc_gemm<256, kATiled3d, false, true, false>(ta, tb, a, di, s_, what);
 }
 

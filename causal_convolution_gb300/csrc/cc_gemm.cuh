@@ -97,7 +97,9 @@ __device__ __forceinline__ void gemm_decode_tile(const GemmArgs& a, int tile, in
 // bias and the shortcut row m added, to high-resolution position
 // (f*epi_tscale + s, 2i+p, 2j+q) of out [frames, 2*img_h, 2*img_w, out_ld] --
 // the interleave done in registers (s = 0 unless the output is x2 in time).
-enum EpiMode : int { kEpiPlain = 0, kEpiResample = 1 };
+// StoreF32: fp32 rows leave in 32-column chunks through a swizzled shared
+// staging buffer and TMA tensor stores (pair kernel only).
+enum EpiMode : int { kEpiPlain = 0, kEpiResample = 1, kEpiStoreF32 = 2 };
 
 template <int EPI>
 __device__ __forceinline__ long long epi_row_offset(const GemmArgs& a, int batch, int m) {

@@ -28,8 +28,9 @@ cc_status launch_tc_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs&
 // overwritten with the number of 256-row pair tiles.
 template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = kEpiPlain>
 cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs& args, const DeviceInfo& di,
-                              cudaStream_t stream, const char* what) {
-  using S = PairShape<BN>;
+                              cudaStream_t stream, const char* what, const CUtensorMap* tc = nullptr) {
+  using S = PairShape<BN, pair_staging_bytes<EPI>()>;
+  if (EPI == kEpiStoreF32 && !tc) return fail(CC_ERR_INVALID, "%s: output tensor map missing", what);
   args.num_tiles = ((args.m_tiles + 1) / 2) * args.n_tiles * args.batches;
   if (args.num_tiles <= 0) return CC_OK;
   auto kern = tc_gemm_pair_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS, EPI>;
@@ -38,7 +39,7 @@ cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, Gemm
   args.err = di.err_word;
   args.timeout_ns = kWaitLimitNs;
   const int pairs = std::min(args.num_tiles, di.sm_count / 2);
-  kern<<<2 * pairs, kGemmThreads, S::kSmemBytes, stream>>>(ta, tb, args);
+  kern<<<2 * pairs, kGemmThreads, S::kSmemBytes, stream>>>(ta, tb, tc ? *tc : tb, args);
   return launch_status(what);
 }
 

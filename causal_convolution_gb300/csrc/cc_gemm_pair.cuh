@@ -19,17 +19,17 @@
 
 namespace cc {
 
-template <int BN>
+template <int BN, int STAGING = 0>  // STAGING: bytes of output staging (TMA-store epilogue)
 struct PairShape {
   static constexpr int kHalfN = BN / 2;
   static constexpr int kABytes = kBlockM * kBlockK * 2;
   static constexpr int kBBytes = kHalfN * kBlockK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;  // per CTA
-  static constexpr int kStagesFit = (232448 - 1024 - 256) / kStageBytes;
+  static constexpr int kStagesFit = (232448 - 1024 - 256 - STAGING) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr uint32_t kAccCols = BN <= 128 ? 128 : 256;
   static constexpr uint32_t kTmemCols = 2 * kAccCols;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + STAGING + 256;
   static_assert(BN % 128 == 0 && BN <= 256, "pair tiles split B into halves of whole 64-column blocks");
   static_assert(kBBytes % 1024 == 0, "B stage must be a whole number of 1024-byte swizzle atoms");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -44,17 +44,26 @@ __device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, in
   mp = r / a.batches;
 }
 
+constexpr int kStoreChunk = 32;                          // fp32 columns per staged TMA store
+constexpr int kStoreBufBytes = kBlockM * kStoreChunk * 4;  // 16 KB: 128 rows x 128 bytes
+
+template <int EPI>
+constexpr int pair_staging_bytes() {
+  return EPI == kEpiStoreF32 ? 2 * kStoreBufBytes : 0;
+}
+
 template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = kEpiPlain>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ GemmArgs args) {
-  using S = PairShape<BN>;
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmArgs args) {
+  using S = PairShape<BN, pair_staging_bytes<EPI>()>;
   constexpr int STAGES = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * S::kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * S::kBBytes);
+  uint8_t* sStage = sB + STAGES * S::kBBytes;  // output staging (TMA-store epilogue only)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + pair_staging_bytes<EPI>());
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -82,6 +91,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
+    if (EPI == kEpiStoreF32) tma_prefetch_map(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), S::kTmemCols);
@@ -209,6 +219,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       mma_commit_pair_both(smem_u32(done));
       (void)mbar_wait(smem_u32(done), 0, args.err, tlim);
     }
+  } else if constexpr (EPI == kEpiStoreF32) {
+    // ------------------------------ epilogue: staged TMA stores (both CTAs) --
+    // Each 32-column chunk of the 128 x BN fp32 tile goes to one of two
+    // swizzled 16 KB shared buffers (row r's 16-byte piece j at j ^ (r & 7)),
+    // then one thread stores it with a TMA tensor store (clipped at the
+    // tensor's edge), so global writes are whole 128-byte rows.
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const bool issuer = (warp == 2 && lane == 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int chunk = 0;
+    for (int tile = pair; tile < args.num_tiles; tile += npairs) {
+      int batch, mp, nt;
+      pair_decode_tile(args, tile, batch, mp, nt);
+      // uniform over the four epilogue warps (shared named barriers below)
+      if (!named_barrier_and(1, 128, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
+      tc_fence_after();
+      const int m0 = (2 * mp + static_cast<int>(rank)) * kBlockM;
+      const int n0 = nt * BN;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * S::kAccCols;
+#pragma unroll 1
+      for (int c = 0; c < BN / kStoreChunk; ++c, ++chunk) {
+        uint32_t r[32];
+        tmem_ld32_wait(tbase + c * kStoreChunk, r);
+        if (c == BN / kStoreChunk - 1) {  // accumulator fully read: release it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+        }
+        uint8_t* buf = sStage + (chunk & 1) * kStoreBufBytes;
+        if (issuer) bulk_wait_read_1();  // the store two chunks back has read this buffer
+        named_barrier_sync(1, 128);
+        uint8_t* rowp = buf + row * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float4*>(rowp + ((j ^ (row & 7)) << 4)) =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                          __uint_as_float(r[4 * j + 3]));
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (issuer) {
+          tma_store_3d(&tmC, smem_u32(buf), n0 + c * kStoreChunk, m0, batch);
+          bulk_commit();
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (issuer) bulk_wait_all();
   } else {
     // --------------------------------------------- epilogue (both CTAs) --
     const int quarter = warp & 3;

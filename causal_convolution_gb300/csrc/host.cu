@@ -138,6 +138,18 @@ cc_status encode_tiled_3d(CUtensorMap* map, const void* base, uint64_t d0, uint6
                        "3-D map");
 }
 
+cc_status encode_tiled_3d_f32_sw128(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                                    uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_result(g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                       "3-D fp32 map");
+}
+
 cc_status encode_tiled_4d_dense(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides[3],
                                 uint32_t box0, uint32_t box1, uint32_t box2) {
   const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
