@@ -526,9 +526,11 @@ def main(argv=None):
             peak = peaks["hbm_gbs"]
             roofs[name] = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                            "ms": per_kernel[name], "work": amount, "in_step": name in KERNELS}
+    traffic = measured_traffic()
+    for name in roofs:
+        roofs[name]["traffic"] = traffic.get(name)  # per-launch DRAM bytes from ncu, None if stale
     dominant = max(KERNELS, key=lambda n: per_kernel[n])
     dr = roofs[dominant]
-    traffic = measured_traffic()
     roofline = {"bound": dr["bound"], "achieved": round(dr["achieved"], 2), "peak": dr["peak"], "unit": dr["unit"],
                 "frac": round(dr["frac"], 4), "traffic": traffic.get(dominant), "kernel": dominant,
                 "peak_source": f"{peaks['source']} ({'burst bf16 GEMM' if dr['bound'] == 'tensor' else 'copy'})"}
@@ -550,6 +552,8 @@ def main(argv=None):
                      "head": per_kernel["head_temporal"] + per_kernel["head_stencil"]},
         "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
                     for n, r in roofs.items()},
+        "traffic_source": "profiles/ncu_traffic.json (per-launch dram read+write of one ncu capture; null when the "
+                          "kernel's sources changed since)",
         "roofline": roofline,
         "e2e": {"value": round(e2e_ms / ws, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": len(KERNELS) * args.steps,
