@@ -238,25 +238,28 @@ class Workload:
         torch.cuda.synchronize(device)
         api.cc_check_device()
 
+    def launches(self, stream):
+        """The hot path as (stage, launch) pairs in launch order, one per entry of KERNELS."""
+        a = self.api
+        return (
+            ("conv", lambda: a.cc_conv3d_causal(self.conv_x, self.conv_wp, self.conv_b, self.conv_y, stream=stream)),
+            ("attn", lambda: a.cc_attn_scores(self.q, self.k, self.s, stream=stream)),
+            ("attn", lambda: a.cc_attn_softmax(self.s, self.p, self.at.hw, self.scale, stream=stream)),
+            ("attn", lambda: a.cc_attn_pv(self.p, self.v, self.o, self.at.hw, stream=stream)),
+            ("res", lambda: a.cc_resample_up2_fused(self.res_x, self.res_pw, self.res_b, self.res_skip,
+                                                    self.res_out, stream=stream)),
+            ("head", lambda: a.cc_head_temporal(self.head_x, self.head_wp, self.g, stream=stream)),
+            ("head", lambda: a.cc_head_stencil(self.g, self.head_b, self.head_out, stream=stream)),
+        )
+
     def step(self, stream, ev=None):
         """The whole hot path once. With `ev` (len(KERNELS)+1 events) each launch is bracketed."""
-        a = self.api
-        rec = (lambda j: ev[j].record(stream)) if ev is not None else (lambda j: None)
-        rec(0)
-        a.cc_conv3d_causal(self.conv_x, self.conv_wp, self.conv_b, self.conv_y, stream=stream)
-        rec(1)
-        a.cc_attn_scores(self.q, self.k, self.s, stream=stream)
-        rec(2)
-        a.cc_attn_softmax(self.s, self.p, self.at.hw, self.scale, stream=stream)
-        rec(3)
-        a.cc_attn_pv(self.p, self.v, self.o, self.at.hw, stream=stream)
-        rec(4)
-        a.cc_resample_up2_fused(self.res_x, self.res_pw, self.res_b, self.res_skip, self.res_out, stream=stream)
-        rec(5)
-        a.cc_head_temporal(self.head_x, self.head_wp, self.g, stream=stream)
-        rec(6)
-        a.cc_head_stencil(self.g, self.head_b, self.head_out, stream=stream)
-        rec(7)
+        if ev is not None:
+            ev[0].record(stream)
+        for j, (_, launch) in enumerate(self.launches(stream)):
+            launch()
+            if ev is not None:
+                ev[j + 1].record(stream)
 
     def rows(self, stream, ev):
         """Rows a4 and a5 as two passes through the phase tensors (3 events)."""
@@ -268,29 +271,81 @@ class Workload:
         ev[2].record(stream)
 
     # ---- end to end through host buffers -------------------------------
-    def host_buffers(self):
+    # Stages in launch order: (inputs copied in, launches, outputs copied back).
+    STAGES = (("conv", ("conv_x",), ("conv_y",)),
+              ("attn", ("q", "k", "v"), ("o",)),
+              ("res", ("res_x", "res_skip"), ("res_out",)),
+              ("head", ("head_x",), ("head_out",)))
+
+    def host_buffers(self, copy_streams: int = 1):
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-        self.h_in = {"conv_x": pin(self.conv_x), "q": pin(self.q), "k": pin(self.k), "v": pin(self.v),
-                     "res_x": pin(self.res_x), "res_skip": pin(self.res_skip), "head_x": pin(self.head_x)}
-        self.h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                      for n, t in (("conv_y", self.conv_y), ("o", self.o), ("res_out", self.res_out),
-                                   ("head_out", self.head_out))}
-        dev_in = {"conv_x": self.conv_x, "q": self.q, "k": self.k, "v": self.v, "res_x": self.res_x,
-                  "res_skip": self.res_skip, "head_x": self.head_x}
-        self.d_in = dev_in
+        self.d_in = {"conv_x": self.conv_x, "q": self.q, "k": self.k, "v": self.v, "res_x": self.res_x,
+                     "res_skip": self.res_skip, "head_x": self.head_x}
+        self.d_out = {"conv_y": self.conv_y, "o": self.o, "res_out": self.res_out, "head_out": self.head_out}
+        self.h_in = {n: pin(t) for n, t in self.d_in.items()}
+        self.h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in self.d_out.items()}
+        dev = self.dev
+        self.s_h2d = [torch.cuda.Stream(dev) for _ in range(copy_streams)]
+        self.s_d2h = [torch.cuda.Stream(dev) for _ in range(copy_streams)]
+        ev = lambda: torch.cuda.Event()
+        nst = len(self.STAGES)
+        self.ev_in = [[ev() for _ in self.s_h2d] for _ in range(nst)]     # stage inputs landed
+        self.ev_used = [ev() for _ in range(nst)]                          # stage kernels done
+        self.ev_out = [[ev() for _ in self.s_d2h] for _ in range(nst)]    # stage outputs read back
+        self.e2e_primed = False
         h2d = sum(t.numel() * t.element_size() for t in self.h_in.values())
         d2h = sum(t.numel() * t.element_size() for t in self.h_out.values())
         return h2d, d2h
 
-    def step_e2e(self, stream):
-        with torch.cuda.stream(stream):
-            for n, t in self.h_in.items():
-                self.d_in[n].copy_(t, non_blocking=True)
-            self.step(stream)
-            self.h_out["conv_y"].copy_(self.conv_y, non_blocking=True)
-            self.h_out["o"].copy_(self.o, non_blocking=True)
-            self.h_out["res_out"].copy_(self.res_out, non_blocking=True)
-            self.h_out["head_out"].copy_(self.head_out, non_blocking=True)
+    @staticmethod
+    def _split(dst, src, k):
+        """k contiguous, element-aligned slices of a copy dst <- src."""
+        a, b = dst.view(-1), src.view(-1)
+        n = a.numel()
+        step = -(-n // k)
+        return [(a[i:i + step], b[i:i + step]) for i in range(0, n, step)]
+
+    def step_e2e(self, stream, h_in=None, h_out=None):
+        """One chunk from pinned host inputs (`h_in`, default the ones
+        `host_buffers` made) to pinned host outputs (`h_out`): the same
+        seven launches as `step`. Inputs go in stage by stage on the copy-in
+        streams, each stage's launches wait only for their own inputs, and each
+        output goes back as soon as its stage ends, so copies overlap compute
+        (and the previous chunk's copies) but never a buffer still in use:
+        a stage's inputs are rewritten only after its kernels of the previous
+        chunk have finished, and its outputs only after they were read back."""
+        h_in = self.h_in if h_in is None else h_in
+        h_out = self.h_out if h_out is None else h_out
+        launches = self.launches(stream)
+        for i, (_, ins, _) in enumerate(self.STAGES):
+            if self.e2e_primed:
+                for s in self.s_h2d:
+                    s.wait_event(self.ev_used[i])
+            for name in ins:
+                for j, (d, h) in enumerate(self._split(self.d_in[name], h_in[name], len(self.s_h2d))):
+                    with torch.cuda.stream(self.s_h2d[j]):
+                        d.copy_(h, non_blocking=True)
+            for j, s in enumerate(self.s_h2d):
+                self.ev_in[i][j].record(s)
+        for i, (stage, _, outs) in enumerate(self.STAGES):
+            for j in range(len(self.s_h2d)):
+                stream.wait_event(self.ev_in[i][j])
+            if self.e2e_primed:
+                for j in range(len(self.s_d2h)):
+                    stream.wait_event(self.ev_out[i][j])
+            for st, launch in launches:
+                if st == stage:
+                    launch()
+            self.ev_used[i].record(stream)
+            for j, s in enumerate(self.s_d2h):
+                s.wait_event(self.ev_used[i])
+            for name in outs:
+                for j, (h, d) in enumerate(self._split(h_out[name], self.d_out[name], len(self.s_d2h))):
+                    with torch.cuda.stream(self.s_d2h[j]):
+                        h.copy_(d, non_blocking=True)
+            for j, s in enumerate(self.s_d2h):
+                self.ev_out[i][j].record(s)
+        self.e2e_primed = True
 
 
 # -------------------------------------------------------------- CPU oracle --
@@ -437,7 +492,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=16.0)
     ap.add_argument("--ref-step-s", type=float, default=4.0)
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -499,7 +554,8 @@ def main(argv=None):
 
     # end to end: host buffers, copies inside the timed region
     h2d, d2h = wl.host_buffers()
-    wl.step_e2e(stream)
+    for _ in range(3):
+        wl.step_e2e(stream)
     torch.cuda.synchronize(device)
     if ws > 1:
         torch.distributed.barrier()
