@@ -41,16 +41,19 @@ WORKLOAD = ("one 4-latent-frame chunk through the four stages: causal conv 1024-
             "attention 4x3432xC1024; resampler 512->512 @ 8x88x156 -> 8x176x312; head 256->12 @ 16x352x624")
 
 # The step: every row of the hot path, with the resampler's phase convs and
-# interleave (rows a4, a5) fused into one kernel.
-KERNELS = ["conv3d_causal", "attn_scores", "attn_softmax", "attn_pv", "resample_up2_fused", "head_temporal",
-           "head_stencil"]
-# Rows a4 and a5 as the two separate passes of the reference design, timed in
-# their own loop after the step (not part of the step's time).
-ROW_KERNELS = ["resample_phase_conv", "resample_interleave"]
+# interleave (rows a4, a5) fused into one kernel and the attention (rows
+# a6-a8) through the key-tile numerators (no fp32 S round trip).
+KERNELS = ["conv3d_causal", "attn_scores_exp", "attn_exp_rescale", "attn_pv_exp", "resample_up2_fused",
+           "head_temporal", "head_stencil"]
+# Rows a4, a5 and a6-a8 as the separate passes of the reference design, timed
+# in their own loop after the step (not part of the step's time).
+ROW_KERNELS = ["resample_phase_conv", "resample_interleave", "attn_scores", "attn_softmax", "attn_pv"]
 
 
-def algorithmic_work():
-    """Per-launch algorithmic work of every kernel: (bound, amount, unit)."""
+def algorithmic_work(rescale_bytes: float = 0.0):
+    """Per-launch algorithmic work of every kernel: (bound, amount, unit).
+    rescale_bytes: what the rescale pass must move for the workload's inputs
+    (it reads and writes only the key tiles not yet on their row's scale)."""
     cv = cc_inputs.CONFIGS["mid_conv"]
     at = cc_inputs.CONFIGS["attention"]
     rs = cc_inputs.CONFIGS["resampler"]
@@ -65,6 +68,9 @@ def algorithmic_work():
         "attn_scores": ("tensor", 2.0 * t * hw * hw * c, "flop"),
         "attn_softmax": ("hbm", t * hw * hw * 4.0 + t * hw * ld * 2.0, "byte"),
         "attn_pv": ("tensor", 2.0 * t * hw * hw * c, "flop"),
+        "attn_scores_exp": ("tensor", 2.0 * t * hw * hw * c, "flop"),
+        "attn_exp_rescale": ("hbm", rescale_bytes, "byte"),
+        "attn_pv_exp": ("tensor", 2.0 * t * hw * hw * c, "flop"),
         "resample_phase_conv": ("tensor", 2.0 * 4 * m_res * rs.cout * 12 * rs.c, "flop"),
         "resample_up2_fused": ("tensor", 2.0 * 4 * m_res * rs.cout * 12 * rs.c, "flop"),
         "resample_interleave": ("hbm", (4 + 1 + 4) * m_res * rs.c * 2.0, "byte"),
@@ -74,7 +80,8 @@ def algorithmic_work():
 
 
 # The source files each kernel is built from (for tying ncu counters to code).
-_GEMM_SRC = ["csrc/cc_gemm.cuh", "csrc/cc_ptx.cuh", "csrc/cc_gemm_launch.cuh", "csrc/cc_host.h", "csrc/host.cu"]
+_GEMM_SRC = ["csrc/cc_gemm.cuh", "csrc/cc_gemm_pair.cuh", "csrc/cc_ptx.cuh", "csrc/cc_gemm_launch.cuh",
+             "csrc/cc_host.h", "csrc/host.cu"]
 KERNEL_SOURCES = {
     "conv3d_causal": _GEMM_SRC + ["csrc/conv.cu"],
     "resample_phase_conv": _GEMM_SRC + ["csrc/conv.cu"],
@@ -83,6 +90,9 @@ KERNEL_SOURCES = {
     "attn_scores": _GEMM_SRC + ["csrc/attn.cu"],
     "attn_pv": _GEMM_SRC + ["csrc/attn.cu"],
     "attn_softmax": ["csrc/attn.cu"],
+    "attn_scores_exp": _GEMM_SRC + ["csrc/attn.cu"],
+    "attn_exp_rescale": ["csrc/attn.cu", "csrc/cc_gemm.cuh"],
+    "attn_pv_exp": _GEMM_SRC + ["csrc/attn.cu"],
     "resample_interleave": ["csrc/passes.cu"],
     "head_stencil": ["csrc/passes.cu"],
 }
@@ -217,6 +227,8 @@ class Workload:
         self.p = E(at.d, at.hw, self.ld)
         self.o = E(at.d, at.hw, at.c)
         self.scale = at.c ** -0.5
+        self.e = E(at.d, at.hw, self.ld)
+        self.st = E(at.d, at.hw, api.cc_attn_exp_key_tiles(at.hw), 2, dt=torch.float32)
 
         rs = cc_inputs.CONFIGS["resampler"]
         i = mk("resampler", device)
@@ -243,9 +255,9 @@ class Workload:
         a = self.api
         return (
             ("conv", lambda: a.cc_conv3d_causal(self.conv_x, self.conv_wp, self.conv_b, self.conv_y, stream=stream)),
-            ("attn", lambda: a.cc_attn_scores(self.q, self.k, self.s, stream=stream)),
-            ("attn", lambda: a.cc_attn_softmax(self.s, self.p, self.at.hw, self.scale, stream=stream)),
-            ("attn", lambda: a.cc_attn_pv(self.p, self.v, self.o, self.at.hw, stream=stream)),
+            ("attn", lambda: a.cc_attn_scores_exp(self.q, self.k, self.e, self.st, self.scale, stream=stream)),
+            ("attn", lambda: a.cc_attn_exp_rescale(self.e, self.st, self.at.hw, stream=stream)),
+            ("attn", lambda: a.cc_attn_pv_exp(self.e, self.st, self.v, self.o, stream=stream)),
             ("res", lambda: a.cc_resample_up2_fused(self.res_x, self.res_pw, self.res_b, self.res_skip,
                                                     self.res_out, stream=stream)),
             ("head", lambda: a.cc_head_temporal(self.head_x, self.head_wp, self.g, stream=stream)),
@@ -262,13 +274,34 @@ class Workload:
                 ev[j + 1].record(stream)
 
     def rows(self, stream, ev):
-        """Rows a4 and a5 as two passes through the phase tensors (3 events)."""
+        """Rows a4, a5 as two passes through the phase tensors and rows a6-a8
+        as three passes through fp32 S and bf16 P (len(ROW_KERNELS)+1 events)."""
         a = self.api
+        launches = (
+            lambda: a.cc_resample_phase_conv(self.res_x, self.res_pw, self.phases, stream=stream),
+            lambda: a.cc_resample_interleave(self.phases, self.res_b, self.res_skip, self.res_out, stream=stream),
+            lambda: a.cc_attn_scores(self.q, self.k, self.s, stream=stream),
+            lambda: a.cc_attn_softmax(self.s, self.p, self.at.hw, self.scale, stream=stream),
+            lambda: a.cc_attn_pv(self.p, self.v, self.o, self.at.hw, stream=stream),
+        )
         ev[0].record(stream)
-        a.cc_resample_phase_conv(self.res_x, self.res_pw, self.phases, stream=stream)
-        ev[1].record(stream)
-        a.cc_resample_interleave(self.phases, self.res_b, self.res_skip, self.res_out, stream=stream)
-        ev[2].record(stream)
+        for j, launch in enumerate(launches):
+            launch()
+            ev[j + 1].record(stream)
+
+    def rescale_bytes(self, stream) -> float:
+        """Bytes the rescale pass moves for these inputs: each key tile whose
+        c_t is below its row's largest is read and written once (bf16), and
+        every row's statistics are read (8 bytes per tile) and those of the
+        rescaled tiles written."""
+        self.api.cc_attn_scores_exp(self.q, self.k, self.e, self.st, self.scale, stream=stream)
+        torch.cuda.synchronize(self.dev)
+        st = self.st.cpu().numpy()
+        c = st[..., 0]
+        moved = c < c.max(axis=2, keepdims=True)
+        tiles = c.shape[2]
+        keys = np.minimum(256, self.at.hw - 256 * np.arange(tiles))  # keys per tile (last one partial)
+        return float(2 * 2 * (moved * keys).sum() + 8 * c.size + 8 * moved.sum())
 
     # ---- end to end through host buffers -------------------------------
     # Stages in launch order: (inputs copied in, launches, outputs copied back).
@@ -542,7 +575,7 @@ def main(argv=None):
     ms_step = max_over_ranks(elapsed / args.steps, device)
 
     # the resampler's two-pass form (rows a4, a5), outside the step
-    rev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    rev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROW_KERNELS) + 1)] for _ in range(args.steps)]
     for _ in range(2):
         wl.rows(stream, rev[0])
     for k in range(args.steps):
@@ -567,7 +600,7 @@ def main(argv=None):
     wl.api.cc_check_device()
 
     peaks = load_peaks()
-    work = algorithmic_work()
+    work = algorithmic_work(wl.rescale_bytes(stream))
     roofs = {}
     for name in KERNELS + ROW_KERNELS:
         bound, amount, unit = work[name]
@@ -602,7 +635,10 @@ def main(argv=None):
         "resampler_interleave_frac_of_hbm": round(roofs["resample_interleave"]["frac"], 4),
         "head_stencil_gbs": round(roofs["head_stencil"]["achieved"], 1),
         "stage_ms": {"conv": per_kernel["conv3d_causal"],
-                     "attention": per_kernel["attn_scores"] + per_kernel["attn_softmax"] + per_kernel["attn_pv"],
+                     "attention": per_kernel["attn_scores_exp"] + per_kernel["attn_exp_rescale"]
+                     + per_kernel["attn_pv_exp"],
+                     "attention_three_pass": per_kernel["attn_scores"] + per_kernel["attn_softmax"]
+                     + per_kernel["attn_pv"],
                      "resampler": per_kernel["resample_up2_fused"],
                      "resampler_two_pass": per_kernel["resample_phase_conv"] + per_kernel["resample_interleave"],
                      "head": per_kernel["head_temporal"] + per_kernel["head_stencil"]},

@@ -38,6 +38,12 @@ SIGNATURES = {
     "cc_attn_softmax": (_I, [_P, _P, _I, _I, _L, _L, _F, _P]),
     "cc_attn_pv": (_I, [_P, _P, _P, _I, _I, _I, _L, _L, _L, _P]),
     "cc_attn_frame": (_I, [_P, _P, _P, _P, _I, _I, _I, _L, _L, _L, _L, _F, _P, _Z, _P]),
+    "cc_attn_exp_key_tiles": (_I, [_I]),
+    "cc_attn_exp_workspace_bytes": (_Z, [_I, _I]),
+    "cc_attn_scores_exp": (_I, [_P, _P, _P, _P, _I, _I, _I, _L, _L, _L, _F, _P]),
+    "cc_attn_exp_rescale": (_I, [_P, _P, _I, _I, _L, _P]),
+    "cc_attn_pv_exp": (_I, [_P, _P, _P, _P, _I, _I, _I, _L, _L, _L, _P]),
+    "cc_attn_frame_exp": (_I, [_P, _P, _P, _P, _I, _I, _I, _L, _L, _L, _L, _F, _P, _Z, _P]),
     "cc_head_prepare": (_I, [_P, _P, _I, _P]),
     "cc_head_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "cc_head_temporal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),

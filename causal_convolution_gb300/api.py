@@ -225,6 +225,61 @@ def cc_attn_frame(q, k, v, o, ws, scale: float | None = None, stream=None) -> No
                                      _stream(stream)))
 
 
+def cc_attn_exp_key_tiles(hw: int) -> int:
+    return _lib.load().cc_attn_exp_key_tiles(hw)
+
+
+def cc_attn_exp_workspace_bytes(t: int, hw: int) -> int:
+    return _lib.load().cc_attn_exp_workspace_bytes(t, hw)
+
+
+def cc_attn_scores_exp(q, k, e, stats, scale: float | None = None, stream=None) -> None:
+    """e: bf16 [T, HW, ld]; stats: fp32 [T, HW, key_tiles, 2] (pairs c_t, l_t)."""
+    t, hw, c, ld_q = _rows(q, "q")
+    _, _, _, ld_k = _rows(k, "k")
+    tiles = cc_attn_exp_key_tiles(hw)
+    if tuple(k.shape) != (t, hw, c) or e.dim() != 3 or tuple(e.shape[:2]) != (t, hw):
+        raise ValueError("attn_scores_exp: shapes do not match")
+    if tuple(stats.shape) != (t, hw, tiles, 2):
+        raise ValueError(f"attn_scores_exp: stats must be [T,HW,{tiles},2]")
+    if scale is None:
+        scale = c ** -0.5
+    _check(_lib.load().cc_attn_scores_exp(q.data_ptr(), k.data_ptr(), _ptr(e, name="e"),
+                                          _ptr(stats, torch.float32, "stats"), t, hw, c, ld_q, ld_k, e.shape[2],
+                                          float(scale), _stream(stream)))
+
+
+def cc_attn_exp_rescale(e, stats, hw: int, stream=None) -> None:
+    t = e.shape[0]
+    if e.dim() != 3 or tuple(e.shape[:2]) != (t, hw) or tuple(stats.shape) != (t, hw, cc_attn_exp_key_tiles(hw), 2):
+        raise ValueError("attn_exp_rescale: e must be [T,HW,ld] and stats [T,HW,key_tiles,2]")
+    _check(_lib.load().cc_attn_exp_rescale(_ptr(e, name="e"), _ptr(stats, torch.float32, "stats"), t, hw, e.shape[2],
+                                           _stream(stream)))
+
+
+def cc_attn_pv_exp(e, stats, v, o, stream=None) -> None:
+    t, hw, c, ld_v = _rows(v, "v")
+    _, _, _, ld_o = _rows(o, "o")
+    if e.dim() != 3 or tuple(e.shape[:2]) != (t, hw) or tuple(stats.shape) != (t, hw, cc_attn_exp_key_tiles(hw), 2):
+        raise ValueError("attn_pv_exp: e must be [T,HW,ld] and stats [T,HW,key_tiles,2]")
+    _check(_lib.load().cc_attn_pv_exp(_ptr(e, name="e"), _ptr(stats, torch.float32, "stats"), v.data_ptr(),
+                                      o.data_ptr(), t, hw, c, e.shape[2], ld_v, ld_o, _stream(stream)))
+
+
+def cc_attn_frame_exp(q, k, v, o, ws, scale: float | None = None, stream=None) -> None:
+    t, hw, c, ld_q = _rows(q, "q")
+    _, _, _, ld_k = _rows(k, "k")
+    _, _, _, ld_v = _rows(v, "v")
+    _, _, _, ld_o = _rows(o, "o")
+    if not (tuple(k.shape) == tuple(v.shape) == tuple(o.shape) == (t, hw, c)):
+        raise ValueError("attn_frame_exp: q, k, v, o must share [T,HW,C]")
+    if scale is None:
+        scale = c ** -0.5
+    _check(_lib.load().cc_attn_frame_exp(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), t, hw, c, ld_q, ld_k,
+                                         ld_v, ld_o, float(scale), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                         _stream(stream)))
+
+
 # -------------------------------------------------------------- output head --
 
 def cc_head_prepare(w, wp, stream=None) -> None:

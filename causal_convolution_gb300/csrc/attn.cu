@@ -261,3 +261,184 @@ extern "C" cc_status cc_attn_frame(const cc_bf16* q, const cc_bf16* k, const cc_
   if ((st = cc_attn_softmax(s, p, t, hw, ld, ld, scale, stream)) != CC_OK) return st;
   return cc_attn_pv(p, v, o, t, hw, c, ld, ld_v, ld_o, stream);
 }
+
+// ------------------------------------------- numerators in key tiles (E) --
+
+namespace cc {
+namespace {
+constexpr int kKeyTile = 256;  // keys per statistics tile = the scores kernel's BN
+constexpr int kRescaleWarps = 8;
+
+// One warp per row: c_row = max_t c_t; every key tile with c_t < c_row is
+// multiplied in place by 2^(c_t - c_row), an exact power of two (lane j takes
+// keys 8j .. 8j+7 of the tile, one 16-byte vector), and its statistics become
+// (c_row, 2^(c_t - c_row) l_t). Tiles already at c_row are not touched. Lane
+// i reads the statistics of tile t0 + i, so the tiles to rescale are known at
+// once and up to kRescaleBatch of them are loaded before any is written.
+constexpr int kRescaleBatch = 8;
+
+__global__ void __launch_bounds__(kRescaleWarps * 32) exp_rescale_kernel(__nv_bfloat16* __restrict__ e,
+                                                                          float2* __restrict__ stats,
+                                                                          long long rows, int hw, long long ld_e,
+                                                                          int tiles) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kRescaleWarps + warp;
+  if (row >= rows) return;
+  float2* st = stats + row * tiles;
+  float c_row = __int_as_float(0xff800000u);
+  for (int t = lane; t < tiles; t += 32) c_row = fmaxf(c_row, st[t].x);
+  c_row = warp_max(c_row);
+  __nv_bfloat16* er = e + row * ld_e;
+  for (int t0 = 0; t0 < tiles; t0 += 32) {
+    const int tl = t0 + lane;
+    const float2 mine = tl < tiles ? st[tl] : make_float2(c_row, 0.f);
+    const float my_al = pow2_nonpos(mine.x - c_row);
+    unsigned todo = __ballot_sync(0xffffffffu, mine.x != c_row);
+    if (mine.x != c_row) st[tl] = make_float2(c_row, mine.y * my_al);
+    while (todo) {  // the same for every lane
+      int tb[kRescaleBatch];
+      uint4 x[kRescaleBatch];
+#pragma unroll
+      for (int i = 0; i < kRescaleBatch; ++i) {
+        tb[i] = -1;
+        if (todo) {
+          tb[i] = __ffs(todo) - 1;
+          todo &= todo - 1;
+        }
+        const int k0 = (t0 + tb[i]) * kKeyTile + 8 * lane;
+        if (tb[i] >= 0 && k0 + 8 <= hw) x[i] = *reinterpret_cast<const uint4*>(er + k0);
+      }
+#pragma unroll
+      for (int i = 0; i < kRescaleBatch; ++i) {
+        const float al = __shfl_sync(0xffffffffu, my_al, tb[i] < 0 ? 0 : tb[i]);
+        if (tb[i] < 0) continue;
+        const int k0 = (t0 + tb[i]) * kKeyTile + 8 * lane;
+        if (k0 + 8 <= hw) {
+          const __nv_bfloat162 al2 = __float2bfloat162_rn(al);
+          __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&x[i]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) h[j] = __hmul2(h[j], al2);
+          *reinterpret_cast<uint4*>(er + k0) = x[i];
+        } else {
+          for (int j = 0; j < 8 && k0 + j < hw; ++j)
+            er[k0 + j] = __float2bfloat16_rn(__bfloat162float(er[k0 + j]) * al);
+        }
+      }
+    }
+  }
+}
+}  // namespace
+}  // namespace cc
+
+extern "C" int cc_attn_exp_key_tiles(int hw) { return hw <= 0 ? 0 : ceil_div(hw, kKeyTile); }
+
+extern "C" size_t cc_attn_exp_workspace_bytes(int t, int hw) {
+  if (t <= 0 || hw <= 0) return 0;
+  const size_t ld = (size_t)cc_attn_ld(hw);
+  return round_up((size_t)t * hw * ld * 2, 256) + round_up((size_t)t * hw * cc_attn_exp_key_tiles(hw) * 8, 256);
+}
+
+extern "C" cc_status cc_attn_scores_exp(const cc_bf16* q, const cc_bf16* k, cc_bf16* e, float* stats, int t, int hw,
+                                        int c, int64_t ld_q, int64_t ld_k, int64_t ld_e, float scale, void* stream) {
+  const char* what = "attn_scores_exp";
+  cc_status st;
+  if ((st = check_ptr(what, q)) != CC_OK || (st = check_ptr(what, k)) != CC_OK || (st = check_ptr(what, e)) != CC_OK ||
+      (st = check_ptr(what, stats)) != CC_OK)
+    return st;
+  if (t <= 0 || hw <= 0 || c <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
+  if (c % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C must be a multiple of 64 (got %d)", what, c);
+  if (ld_q < c || ld_k < c || ld_e < hw) return fail(CC_ERR_INVALID, "%s: row strides too small", what);
+  if (ld_q % 8 || ld_k % 8 || ld_e % 8) return fail(CC_ERR_INVALID, "%s: row strides must be multiples of 8", what);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CC_ERR_INVALID, "%s: scale must be finite and > 0", what);
+  DeviceInfo di;
+  if ((st = device_info(&di)) != CC_OK) return st;
+  CUtensorMap ta, tb, tc;
+  if ((st = encode_tiled_3d(&ta, q, c, hw, t, 2ull * ld_q, 2ull * ld_q * hw, kBlockK, kBlockM)) != CC_OK) return st;
+  if ((st = encode_tiled_3d(&tb, k, c, hw, t, 2ull * ld_k, 2ull * ld_k * hw, kBlockK, 128)) != CC_OK) return st;
+  // E leaves through TMA tensor stores of 64-key x 128-row bf16 boxes
+  if ((st = encode_tiled_3d(&tc, e, hw, hw, t, 2ull * ld_e, 2ull * ld_e * hw, kBlockK, kBlockM)) != CC_OK) return st;
+  GemmArgs a{};
+  a.m_total = hw;
+  a.n_total = hw;
+  a.m_tiles = ceil_div(hw, kBlockM);
+  a.n_tiles = ceil_div(hw, kKeyTile);
+  a.batches = t;
+  a.num_tiles = a.m_tiles * a.n_tiles * t;
+  a.taps = 1;
+  a.kb_per_tap = c / kBlockK;
+  a.out = e;
+  a.out_ld = ld_e;
+  a.out_batch = (long long)hw * ld_e;
+  a.stats = reinterpret_cast<float2*>(stats);
+  a.stat_tiles = a.n_tiles;
+  a.exp_k = scale * 1.4426950408889634f;
+  return launch_tc_gemm_pair<kKeyTile, kATiled3d, false, false, false, kEpiExpBf16>(
+      ta, tb, a, di, static_cast<cudaStream_t>(stream), what, &tc);
+}
+
+extern "C" cc_status cc_attn_exp_rescale(cc_bf16* e, float* stats, int t, int hw, int64_t ld_e, void* stream) {
+  const char* what = "attn_exp_rescale";
+  cc_status st;
+  if ((st = check_ptr(what, e)) != CC_OK || (st = check_ptr(what, stats)) != CC_OK) return st;
+  if (t <= 0 || hw <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
+  if (ld_e < hw || ld_e % 8) return fail(CC_ERR_INVALID, "%s: need ld_e >= HW and ld_e %% 8 == 0", what);
+  DeviceInfo di;
+  if ((st = device_info(&di)) != CC_OK) return st;
+  const long long rows = (long long)t * hw;
+  const unsigned grid = (unsigned)((rows + kRescaleWarps - 1) / kRescaleWarps);
+  exp_rescale_kernel<<<grid, kRescaleWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<__nv_bfloat16*>(e), reinterpret_cast<float2*>(stats), rows, hw, ld_e,
+      cc_attn_exp_key_tiles(hw));
+  return launch_status(what);
+}
+
+extern "C" cc_status cc_attn_pv_exp(const cc_bf16* e, const float* stats, const cc_bf16* v, cc_bf16* o, int t, int hw,
+                                    int c, int64_t ld_e, int64_t ld_v, int64_t ld_o, void* stream) {
+  const char* what = "attn_pv_exp";
+  cc_status st;
+  if ((st = check_ptr(what, e)) != CC_OK || (st = check_ptr(what, stats)) != CC_OK ||
+      (st = check_ptr(what, v)) != CC_OK || (st = check_ptr(what, o)) != CC_OK)
+    return st;
+  if (t <= 0 || hw <= 0 || c <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
+  if (c % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C must be a multiple of 64 (got %d)", what, c);
+  if (ld_e < hw || ld_v < c || ld_o < c) return fail(CC_ERR_INVALID, "%s: row strides too small", what);
+  if (ld_e % 8 || ld_v % 8 || ld_o % 8) return fail(CC_ERR_INVALID, "%s: row strides must be multiples of 8", what);
+  DeviceInfo di;
+  if ((st = device_info(&di)) != CC_OK) return st;
+  CUtensorMap ta, tb;
+  if ((st = encode_tiled_3d(&ta, e, hw, hw, t, 2ull * ld_e, 2ull * ld_e * hw, kBlockK, kBlockM)) != CC_OK) return st;
+  if ((st = encode_tiled_3d(&tb, v, c, hw, t, 2ull * ld_v, 2ull * ld_v * hw, 64, kBlockK)) != CC_OK) return st;
+  GemmArgs a{};
+  a.m_total = hw;
+  a.n_total = c;
+  a.m_tiles = ceil_div(hw, kBlockM);
+  a.n_tiles = ceil_div(c, 256);
+  a.batches = t;
+  a.num_tiles = a.m_tiles * a.n_tiles * t;
+  a.taps = 1;
+  a.kb_per_tap = ceil_div(hw, kBlockK);
+  a.out = o;
+  a.out_ld = ld_o;
+  a.out_batch = (long long)hw * ld_o;
+  a.stats = const_cast<float2*>(reinterpret_cast<const float2*>(stats));
+  a.stat_tiles = cc_attn_exp_key_tiles(hw);
+  return launch_tc_gemm_pair<256, kATiled3d, true, false, false, kEpiRowScale>(ta, tb, a, di,
+                                                                              static_cast<cudaStream_t>(stream), what);
+}
+
+extern "C" cc_status cc_attn_frame_exp(const cc_bf16* q, const cc_bf16* k, const cc_bf16* v, cc_bf16* o, int t, int hw,
+                                       int c, int64_t ld_q, int64_t ld_k, int64_t ld_v, int64_t ld_o, float scale,
+                                       void* ws, size_t ws_bytes, void* stream) {
+  const char* what = "attn_frame_exp";
+  if (t <= 0 || hw <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
+  cc_status st = check_ptr(what, ws);
+  if (st != CC_OK) return st;
+  const size_t need = cc_attn_exp_workspace_bytes(t, hw);
+  if (ws_bytes < need) return fail(CC_ERR_INVALID, "%s: workspace of %zu bytes, need %zu", what, ws_bytes, need);
+  const int64_t ld = cc_attn_ld(hw);
+  cc_bf16* e = static_cast<cc_bf16*>(ws);
+  float* stats = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up((size_t)t * hw * ld * 2, 256));
+  if ((st = cc_attn_scores_exp(q, k, e, stats, t, hw, c, ld_q, ld_k, ld, scale, stream)) != CC_OK) return st;
+  if ((st = cc_attn_exp_rescale(e, stats, t, hw, ld, stream)) != CC_OK) return st;
+  return cc_attn_pv_exp(e, stats, v, o, t, hw, c, ld, ld_v, ld_o, stream);
+}

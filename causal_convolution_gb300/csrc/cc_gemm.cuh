@@ -59,6 +59,11 @@ struct GemmArgs {
   const __nv_bfloat16* bias;  // per column, or nullptr
   const __nv_bfloat16* skip;  // resampler epilogue: shortcut rows (row m at m * out_ld)
   int epi_tscale;             // resampler epilogue: 2 when the output is also x2 in time
+  // softmax numerators in key tiles (kEpiExpBf16 writes them, kEpiRowScale
+  // reads them): per (batch, row, key tile) the pair (c_t, l_t)
+  float2* stats;
+  int stat_tiles;   // key tiles per row
+  float exp_k;      // scale * log2(e): exp(scale * s) = exp2(exp_k * s)
   unsigned int* err;
   unsigned long long timeout_ns;
 };
@@ -99,7 +104,42 @@ __device__ __forceinline__ void gemm_decode_tile(const GemmArgs& a, int tile, in
 // the interleave done in registers (s = 0 unless the output is x2 in time).
 // StoreF32: fp32 rows leave in 32-column chunks through a swizzled shared
 // staging buffer and TMA tensor stores (pair kernel only).
-enum EpiMode : int { kEpiPlain = 0, kEpiResample = 1, kEpiStoreF32 = 2 };
+// ExpBf16 (pair kernel only): the tile holds scores s of one row against BN
+// keys; per row, with c_t = ceil(exp_k * max over the tile's valid keys),
+// e = exp2(exp_k * s - c_t) in (0, 1] leaves as bf16 through the same staged
+// TMA stores, and (c_t, l_t = sum of the fp32 e) goes to stats.
+// RowScale: plain rows multiplied by 1 / l_row, l_row = sum_t 2^(c_t - c_row) l_t.
+enum EpiMode : int { kEpiPlain = 0, kEpiResample = 1, kEpiStoreF32 = 2, kEpiExpBf16 = 3, kEpiRowScale = 4 };
+
+// 2^e for an integer-valued e <= 0, exactly (0 below the normal range).
+__device__ __forceinline__ float pow2_nonpos(float e) {
+  return e <= -127.f ? 0.f : __int_as_float((127 + static_cast<int>(e)) << 23);
+}
+
+// max_t c_t over a row's key-tile statistics (four loads in flight).
+__device__ __forceinline__ float row_max_c(const float2* st, int tiles) {
+  float m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = __int_as_float(0xff800000u);  // -inf
+  int t = 0;
+  for (; t + 4 <= tiles; t += 4) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], st[t + i].x);
+  }
+  for (; t < tiles; ++t) m[0] = fmaxf(m[0], st[t].x);
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// c_row and l_row of one row from its key-tile statistics.
+__device__ __forceinline__ void row_stats(const GemmArgs& a, int batch, int m, float& c_row, float& l_row) {
+  const float2* st = a.stats + (static_cast<long long>(batch) * a.m_total + m) * a.stat_tiles;
+  c_row = row_max_c(st, a.stat_tiles);
+  l_row = 0.f;
+  for (int t = 0; t < a.stat_tiles; ++t) {
+    const float2 v = st[t];
+    l_row += v.y * pow2_nonpos(v.x - c_row);
+  }
+}
 
 template <int EPI>
 __device__ __forceinline__ long long epi_row_offset(const GemmArgs& a, int batch, int m) {
@@ -134,7 +174,7 @@ __device__ __forceinline__ void add_bf16x16(float (&v)[16], const __nv_bfloat16*
 // (skip row at soff): + bias, + shortcut, one rounding (or fp32 as is).
 template <bool OUT_F32, bool HAS_BIAS, int EPI>
 __device__ __forceinline__ void epi_store16(const GemmArgs& a, long long roff, long long soff, int n,
-                                            const uint32_t (&r)[16]) {
+                                            const uint32_t (&r)[16], float rscale = 1.f) {
   const bool full_chunk = n + 16 <= a.n_total;
   if constexpr (OUT_F32) {
     float* o = static_cast<float*>(a.out) + roff + n;
@@ -151,7 +191,7 @@ __device__ __forceinline__ void epi_store16(const GemmArgs& a, long long roff, l
   } else {
   float v[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) * (EPI == kEpiRowScale ? rscale : 1.f);
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + roff + n;
   if (full_chunk) {
     if (HAS_BIAS) add_bf16x16(v, a.bias + n);

@@ -30,7 +30,8 @@ template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = k
 cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs& args, const DeviceInfo& di,
                               cudaStream_t stream, const char* what, const CUtensorMap* tc = nullptr) {
   using S = PairShape<BN, pair_staging_bytes<EPI>()>;
-  if (EPI == kEpiStoreF32 && !tc) return fail(CC_ERR_INVALID, "%s: output tensor map missing", what);
+  if ((EPI == kEpiStoreF32 || EPI == kEpiExpBf16) && !tc)
+    return fail(CC_ERR_INVALID, "%s: output tensor map missing", what);
   args.num_tiles = ((args.m_tiles + 1) / 2) * args.n_tiles * args.batches;
   if (args.num_tiles <= 0) return CC_OK;
   auto kern = tc_gemm_pair_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS, EPI>;

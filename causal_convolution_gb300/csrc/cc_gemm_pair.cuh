@@ -49,7 +49,7 @@ constexpr int kStoreBufBytes = kBlockM * kStoreChunk * 4;  // 16 KB: 128 rows x 
 
 template <int EPI>
 constexpr int pair_staging_bytes() {
-  return EPI == kEpiStoreF32 ? 2 * kStoreBufBytes : 0;
+  return (EPI == kEpiStoreF32 || EPI == kEpiExpBf16) ? 2 * kStoreBufBytes : 0;
 }
 
 template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = kEpiPlain>
@@ -91,7 +91,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
-    if (EPI == kEpiStoreF32) tma_prefetch_map(&tmC);
+    if (EPI == kEpiStoreF32 || EPI == kEpiExpBf16) tma_prefetch_map(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), S::kTmemCols);
@@ -219,6 +219,102 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       mma_commit_pair_both(smem_u32(done));
       (void)mbar_wait(smem_u32(done), 0, args.err, tlim);
     }
+  } else if constexpr (EPI == kEpiExpBf16) {
+    // ------------- epilogue: softmax numerators per key tile (both CTAs) --
+    // Two passes over the row's BN accumulator columns: the max over the
+    // valid keys, then e = exp2(exp_k * s - c_t) packed to bf16 in 64-column
+    // chunks through the swizzled staging buffers and TMA stores (as in
+    // StoreF32), with l_t summed from the fp32 e.
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const bool issuer = (warp == 2 && lane == 0);
+    const float kx = args.exp_k;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int chunk = 0;
+    for (int tile = pair; tile < args.num_tiles; tile += npairs) {
+      int batch, mp, nt;
+      pair_decode_tile(args, tile, batch, mp, nt);
+      if (!named_barrier_and(1, 128, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
+      tc_fence_after();
+      const int m0 = (2 * mp + static_cast<int>(rank)) * kBlockM;
+      const int n0 = nt * BN;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * S::kAccCols;
+      // chunks holding at least one valid key (the same for every thread)
+      const int valid = args.n_total - n0;
+      const int c32_end = valid >= BN ? BN / 32 : (valid + 31) / 32;
+      const int c64_end = valid >= BN ? BN / 64 : (valid + 63) / 64;
+      float m4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m4[i] = __int_as_float(0xff800000u);
+#pragma unroll 1
+      for (int c = 0; c < c32_end; ++c) {
+        uint32_t r[32];
+        tmem_ld32_wait(tbase + c * 32, r);
+        const int nb = n0 + c * 32;
+        if (nb + 32 <= args.n_total) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(r[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (nb + j < args.n_total) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(r[j]));
+        }
+      }
+      const float ct = ceilf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * kx);
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int c = 0; c < c64_end; ++c, ++chunk) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32_wait(tbase + c * 64, r0);
+        tmem_ld32_wait(tbase + c * 64 + 32, r1);
+        if (c == c64_end - 1) {  // accumulator fully read: release it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+        }
+        const int nb = n0 + c * 64;
+        const bool full_chunk = nb + 64 <= args.n_total;
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t s0 = j < 16 ? r0[2 * j] : r1[2 * j - 32];
+          const uint32_t s1 = j < 16 ? r0[2 * j + 1] : r1[2 * j - 31];
+          float e0 = ex2_approx(fmaf(__uint_as_float(s0), kx, -ct));
+          float e1 = ex2_approx(fmaf(__uint_as_float(s1), kx, -ct));
+          if (!full_chunk) {
+            e0 = nb + 2 * j < args.n_total ? e0 : 0.f;
+            e1 = nb + 2 * j + 1 < args.n_total ? e1 : 0.f;
+          }
+          l4[j & 3] += e0 + e1;
+          __nv_bfloat162 b = __floats2bfloat162_rn(e0, e1);
+          pk[j] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        uint8_t* buf = sStage + (chunk & 1) * kStoreBufBytes;
+        if (issuer) bulk_wait_read_1();  // the store two chunks back has read this buffer
+        named_barrier_sync(1, 128);
+        uint8_t* rowp = buf + row * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(rowp + ((j ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (issuer) {
+          tma_store_3d(&tmC, smem_u32(buf), nb, m0, batch);
+          bulk_commit();
+        }
+      }
+      const float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+      const int m = m0 + row;
+      if (m < args.m_total)
+        args.stats[(static_cast<long long>(batch) * args.m_total + m) * args.stat_tiles + nt] = make_float2(ct, l);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (issuer) bulk_wait_all();
   } else if constexpr (EPI == kEpiStoreF32) {
     // ------------------------------ epilogue: staged TMA stores (both CTAs) --
     // Each 32-column chunk of the 128 x BN fp32 tile goes to one of two
@@ -289,6 +385,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * S::kAccCols;
       const long long roff = row_ok ? epi_row_offset<EPI>(args, batch, m) : 0;
       const long long soff = static_cast<long long>(m) * args.out_ld;
+      float rscale = 1.f;
+      if constexpr (EPI == kEpiRowScale) {
+        if (row_ok) {
+          float c_row, l_row;
+          row_stats(args, batch, m, c_row, l_row);
+          rscale = 1.f / l_row;
+        }
+      }
 #pragma unroll 1
       for (int c = 0; c < BN; c += 16) {
         uint32_t r[16];
@@ -296,7 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tmem_ld16(tbase + c, r);
         tmem_wait16(r);
         const int n = n0 + c;
-        if (row_ok && n < args.n_total) epi_store16<OUT_F32, HAS_BIAS, EPI>(args, roff, soff, n, r);
+        if (row_ok && n < args.n_total) epi_store16<OUT_F32, HAS_BIAS, EPI>(args, roff, soff, n, r, rscale);
       }
       tc_fence_before();
       __syncwarp();

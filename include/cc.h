@@ -182,6 +182,51 @@ cc_status cc_attn_frame(const cc_bf16* q, const cc_bf16* k, const cc_bf16* v, cc
                         int64_t ld_q, int64_t ld_k, int64_t ld_v, int64_t ld_o, float scale, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* Attention without the fp32 S round trip and the softmax pass, for the same
+ * result as cc_attn_frame (softmax per row, [ATTN]), in three launches:
+ *  1. cc_attn_scores_exp keeps each 128 x 256 tile of S in TMEM and writes,
+ *     per row i and key tile t = j / 256, the numerators
+ *     E[f,i,j] = bf16( exp2(kx * S[f,i,j] - c_t) ), kx = scale * log2(e),
+ *     c_t = ceil(kx * max of the row's S over the tile), so every E is in
+ *     (0, 1]; and the row statistics (c_t, l_t), l_t = sum over the tile of
+ *     the unrounded exponentials.
+ *  2. cc_attn_exp_rescale puts every row on one scale: c_row = max_t c_t, and
+ *     each tile with c_t < c_row is multiplied in place by the exact power of
+ *     two 2^(c_t - c_row), its statistics becoming (c_row, 2^(c_t - c_row) l_t).
+ *  3. cc_attn_pv_exp computes O = E v with fp32 accumulation and scales each
+ *     output row by 1 / l_row, l_row = sum_t l_t.
+ * P = E / l_row is then the softmax of the row; E is rounded once, as P is in
+ * cc_attn_softmax. */
+
+/* Key tiles per row: ceil(HW / 256). */
+int cc_attn_exp_key_tiles(int hw);
+
+/* Bytes of workspace cc_attn_frame_exp needs: E bf16 [T, HW, cc_attn_ld(HW)]
+ * and the statistics, float pairs [T, HW, cc_attn_exp_key_tiles(HW)]. */
+size_t cc_attn_exp_workspace_bytes(int t, int hw);
+
+/* Step 1 from q, k [T, HW, C] (row strides ld_q, ld_k elements). e: row
+ * stride ld_e elements (ld_e >= HW, % 8 == 0; keys HW .. ld_e-1 are not
+ * written); stats: T*HW*cc_attn_exp_key_tiles(HW) pairs (c_t, l_t),
+ * row-major [T][HW][tiles]. Needs C % 64 == 0, scale finite and > 0. */
+cc_status cc_attn_scores_exp(const cc_bf16* q, const cc_bf16* k, cc_bf16* e, float* stats, int t, int hw, int c,
+                             int64_t ld_q, int64_t ld_k, int64_t ld_e, float scale, void* stream);
+
+/* Step 2, in place on e and stats (as written by step 1). */
+cc_status cc_attn_exp_rescale(cc_bf16* e, float* stats, int t, int hw, int64_t ld_e, void* stream);
+
+/* Step 3: O[f,i,:] = sum_j E[f,i,j] v[f,j,:] / l_row for E and statistics on
+ * one scale per row (after step 2); v read as stored ([j][c]). Needs
+ * C % 64 == 0, ld_e, ld_v, ld_o % 8 == 0. */
+cc_status cc_attn_pv_exp(const cc_bf16* e, const float* stats, const cc_bf16* v, cc_bf16* o, int t, int hw, int c,
+                         int64_t ld_e, int64_t ld_v, int64_t ld_o, void* stream);
+
+/* Steps 1-3: the same contract as cc_attn_frame with a workspace of
+ * cc_attn_exp_workspace_bytes(). */
+cc_status cc_attn_frame_exp(const cc_bf16* q, const cc_bf16* k, const cc_bf16* v, cc_bf16* o, int t, int hw, int c,
+                            int64_t ld_q, int64_t ld_k, int64_t ld_v, int64_t ld_o, float scale, void* ws,
+                            size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------ output head [HEAD] */
 
 #define CC_HEAD_COUT 12

@@ -57,6 +57,9 @@ def test_version_and_workspace_arithmetic(lib):
     ld = 3432
     assert lib.cc_attn_workspace_bytes(4, 3432) == 4 * 3432 * ld * 4 + 4 * 3432 * ld * 2
     assert lib.cc_resample_workspace_bytes(0, 1, 1, 1, 1) == 0
+    assert lib.cc_attn_exp_key_tiles(3432) == 14
+    assert lib.cc_attn_exp_key_tiles(256) == 1 and lib.cc_attn_exp_key_tiles(257) == 2
+    assert lib.cc_attn_exp_workspace_bytes(4, 3432) == 4 * 3432 * ld * 2 + 4 * 3432 * 14 * 8
 
 
 def test_host_validation_rejects_before_any_launch(lib):
@@ -77,5 +80,13 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert lib.cc_attn_frame(p, p, p, p, 1, 16, 64, 64, 64, 64, 64, ctypes.c_float(0.125), p, 16, None) == 1
     assert b"workspace" in lib.cc_last_error()
     assert lib.cc_head_out(p, p, p, p, 1, 1, 4, 4, 64, 0, p, 10, None) == 1
+    assert lib.cc_attn_scores_exp(p, p, p, None, 1, 16, 64, 64, 64, 16, ctypes.c_float(0.125), None) == 1
+    assert b"null" in lib.cc_last_error()
+    assert lib.cc_attn_scores_exp(p, p, p, p, 1, 16, 64, 64, 64, 16, ctypes.c_float(0.0), None) == 1  # scale
+    assert lib.cc_attn_scores_exp(p, p, p, p, 1, 16, 48, 48, 48, 16, ctypes.c_float(0.125), None) == 2  # C % 64
+    assert lib.cc_attn_pv_exp(p, p + 4, p, p, 1, 16, 64, 16, 64, 64, None) == 1  # stats misaligned
+    assert lib.cc_attn_exp_rescale(p, p, 1, 16, 12, None) == 1  # ld_e % 8
+    assert lib.cc_attn_frame_exp(p, p, p, p, 1, 16, 64, 64, 64, 64, 64, ctypes.c_float(0.125), p, 16, None) == 1
+    assert b"workspace" in lib.cc_last_error()
     assert lib.cc_debug_wait_timeout(0, None) == 1
     assert lib.cc_debug_im2col_tile(p, p, 1, 1, 1, 1, 64, -17, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == 1
