@@ -394,11 +394,18 @@ def oracle_sample_step(cpu, budget_s: float, rng):
     desc = []
     per_stage = budget_s / 4.0
 
-    def timed(fn, npts, total):
-        t0 = time.perf_counter()
-        fn(npts)
-        dt = time.perf_counter() - t0
-        return dt, dt * total / npts
+    def timed(fn, total):
+        """Batches of sampled outputs (8 to 4096 per call) until the stage's
+        share of the budget is spent; returns (points, seconds, ms per chunk)."""
+        npts, dt, n = 0, 0.0, 8
+        while True:
+            t0 = time.perf_counter()
+            fn(n)
+            dt += time.perf_counter() - t0
+            npts += n
+            if dt >= per_stage:
+                return npts, dt, dt * total / npts * 1e3
+            n = int(min(4096, max(8, (per_stage - dt) * npts / dt)))
 
     stages = []
     cv = cc_inputs.CONFIGS["mid_conv"]
@@ -419,14 +426,9 @@ def oracle_sample_step(cpu, budget_s: float, rng):
                    lambda P: oracle.head_out_at(cpu["head_x"], cpu["head_w"], cpu["head_b"],
                                                 _pts(rng, P, hd.n, hf, hd.h, hd.w))))
     for name, total, fn in stages:
-        npts = 8
-        dt, ms = timed(fn, npts, total)
+        npts, dt, ms = timed(fn, total)
         spent += dt
-        if dt < per_stage / 4:
-            npts = int(min(4096, max(8, npts * per_stage / max(dt, 1e-4))))
-            dt, ms = timed(fn, npts, total)
-            spent += dt
-        total_ms += ms * 1e3
+        total_ms += ms
         desc.append(f"{name}: {npts} of {total} outputs")
     return total_ms, spent, "; ".join(desc) + " (extrapolated by output count)"
 
@@ -494,12 +496,14 @@ def run_reference(args):
     device = "cuda:0" if torch.cuda.is_available() else "cpu"
     cpu = host_inputs(device)
     rng = np.random.default_rng(0)
+    # each step a bounded sample: the whole run stays near --ref-total-s
+    step_s = min(args.ref_step_s, args.ref_total_s / (args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample_step(cpu, args.ref_step_s, rng)
+        oracle_sample_step(cpu, step_s, rng)
     vals, spent, desc = [], 0.0, ""
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        v, s, desc = oracle_sample_step(cpu, args.ref_step_s, rng)
+        v, s, desc = oracle_sample_step(cpu, step_s, rng)
         vals.append(v)
         spent += s
     wall = time.perf_counter() - t0
@@ -525,6 +529,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=16.0)
     ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--ref-total-s", type=float, default=150.0)
     ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args(argv)
     if args.warmup < 3:
