@@ -14,9 +14,15 @@
 //    last (kt = 2) frame has been multiplied in.
 //  - CTAs work in pairs (cta_group::2): a pair owns two neighbouring tiles,
 //    each CTA streams its own tile and keeps half of the weight's rows
-//    (56 of each tap's 112, 86 KB), so 8 A stages (128 KB) fit beside it and
+//    (56 of each tap's 112, 86 KB), so 6 A stages (96 KB) fit beside it and
 //    enough input is in flight to run at the copy bandwidth; one
 //    tcgen05.mma.cta_group::2 (M=256, N=112) from the even CTA covers both.
+//  - The work is the sequence of (tile pair, output frame) items, split into
+//    equal contiguous shares, one per CTA pair: a share may start or end in
+//    the middle of a tile pair's frames (a segment), and a segment that starts
+//    at output u0 re-reads the (up to two) input frames before it that
+//    output u0 needs. Whole tile pairs per CTA pair would leave the last
+//    wave a quarter full at the bench size (858 tile pairs on 76 CTA pairs).
 // Warp 0 streams A with TMA, warp 1 of the even CTA issues the MMAs, warps 2-5
 // of both CTAs drain accumulators to bf16 g. Every wait is bounded.
 #include <cuda_bf16.h>
@@ -42,6 +48,7 @@ struct HeadArgs {
   int plane_tiles;  // 128-position tiles per frame
   int pair_tiles;   // pairs of tiles per frame: ceil(plane_tiles / 2)
   int units;        // images x pair_tiles
+  long long work;   // units x d_out: (tile pair, output frame) items
   int d_in;         // frames of x per image (D + hist)
   int d_out;        // output frames per image
   int hist;         // 0 or 2
@@ -67,6 +74,18 @@ struct HeadShape {
 
 // First frame of x that contributes to output u.
 __device__ __forceinline__ int first_frame(int u, int hist) { return max(0, u + hist - 2); }
+
+// The next segment of this CTA pair's share [*g, end) of the work items:
+// outputs u0 .. u1-1 of tile pair `unit`. False when the share is done.
+__device__ __forceinline__ bool next_segment(const HeadArgs& a, long long& g, long long end, int& unit, int& u0,
+                                             int& u1) {
+  if (g >= end) return false;
+  unit = static_cast<int>(g / a.d_out);
+  u0 = static_cast<int>(g - static_cast<long long>(unit) * a.d_out);
+  u1 = static_cast<int>(min(static_cast<long long>(a.d_out), u0 + (end - g)));
+  g += u1 - u0;
+  return true;
+}
 
 template <int CB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
@@ -94,6 +113,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
+  const long long share_begin = a.work * pair / npairs;
+  const long long share_end = a.work * (pair + 1) / npairs;
   if (threadIdx.x == 0) {
     for (int s = 0; s < AST; ++s) {
       mbar_init(smem_u32(&afull[s]), 1);
@@ -133,10 +154,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int unit = pair; ok && unit < a.units; unit += npairs) {
+      long long gi = share_begin;
+      int unit, u0, u1;
+      while (ok && next_segment(a, gi, share_end, unit, u0, u1)) {
         const int img = unit / a.pair_tiles;
         const int m0 = (2 * (unit - img * a.pair_tiles) + static_cast<int>(rank)) * kBlockM;
-        for (int f = 0; ok && f < a.d_in; ++f) {
+        for (int f = first_frame(u0, a.hist); ok && f < u1 + a.hist; ++f) {
           for (int kb = 0; kb < CB; ++kb) {
             if (!mbar_wait(smem_u32(&aempty[stage]), phase ^ 1u, a.err, tlim)) {
               ok = false;
@@ -173,13 +196,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       int stage = 0;
       uint32_t phase = 0;
-      int q_base = 0;  // sequence number of this unit's output 0 among this CTA's outputs
-      for (int unit = pair; ok && unit < a.units; unit += npairs) {
-        for (int f = 0; ok && f < a.d_in; ++f) {
+      int q_base = 0;  // sequence number of the segment's output u0 among this CTA's outputs, minus u0
+      long long gi = share_begin;
+      int unit, u0, u1;
+      while (ok && next_segment(a, gi, share_end, unit, u0, u1)) {
+        q_base -= u0;
+        for (int f = first_frame(u0, a.hist); ok && f < u1 + a.hist; ++f) {
           // Outputs this frame starts must have their accumulator slot drained.
           for (int kt = 0; kt < 3; ++kt) {
             const int u = f - a.hist + 2 - kt;
-            if (u < 0 || u >= a.d_out || f != first_frame(u, a.hist)) continue;
+            if (u < u0 || u >= u1 || f != first_frame(u, a.hist)) continue;
             const int q = q_base + u;
             if (!mbar_wait(smem_u32(&tempty[q & 3]), ((q >> 2) & 1) ^ 1u, a.err, tlim)) {
               ok = false;
@@ -195,7 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int kt = 0; kt < 3; ++kt) {
             const int u = f - a.hist + 2 - kt;
-            live[kt] = u >= 0 && u < a.d_out;
+            live[kt] = u >= u0 && u < u1;
             starts[kt] = live[kt] && f == first_frame(u, a.hist);
             d_col[kt] = tmem_base + ((q_base + u) & 3) * kHeadAccCols;
           }
@@ -224,9 +250,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
           if (!ok) break;
           const int u_done = f - a.hist;  // its kt = 2 frame was the last one
-          if (u_done >= 0 && u_done < a.d_out) mma_commit_pair_both(smem_u32(&tfull[(q_base + u_done) & 3]));
+          if (u_done >= u0 && u_done < u1) mma_commit_pair_both(smem_u32(&tfull[(q_base + u_done) & 3]));
         }
-        q_base += a.d_out;
+        q_base += u1;
       }
       mma_commit_pair_both(smem_u32(done));
       (void)mbar_wait(smem_u32(done), 0, a.err, tlim);
@@ -242,11 +268,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     uint8_t* my_row = sOut + row * (kHeadN * 2);
     int q = 0;
     bool ok = true;
-    for (int unit = pair; ok && unit < a.units; unit += npairs) {
+    long long gi = share_begin;
+    int unit, u0, u1;
+    while (ok && next_segment(a, gi, share_end, unit, u0, u1)) {
       const int img = unit / a.pair_tiles;
       const int m0 = (2 * (unit - img * a.pair_tiles) + static_cast<int>(rank)) * kBlockM;
       const int rows = min(kBlockM, a.plane - m0);  // may be <= 0 for the odd CTA of the last pair
-      for (int u = 0; u < a.d_out; ++u, ++q) {
+      for (int u = u0; u < u1; ++u, ++q) {
         const int slot = q & 3;
         // uniform over the four epilogue warps: they leave together, since
         // they share .sync.aligned TMEM loads and named barriers
@@ -330,7 +358,8 @@ cc_status launch_head_temporal(const CUtensorMap& tx, const CUtensorMap& tw, Hea
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "head_temporal: shared-memory attribute: %s", cudaGetErrorString(e));
   a.err = di.err_word;
   a.timeout_ns = kWaitLimitNs;
-  kern<<<2 * std::min(a.units, di.sm_count / 2), kGemmThreads, S::kSmemBytes, stream>>>(tx, tw, a);
+  kern<<<2 * static_cast<int>(std::min<long long>(a.work, di.sm_count / 2)), kGemmThreads, S::kSmemBytes, stream>>>(
+      tx, tw, a);
   return launch_status("head_temporal");
 }
 
@@ -378,6 +407,7 @@ extern "C" cc_status cc_head_temporal(const cc_bf16* x, const cc_bf16* wp, cc_bf
   a.plane_tiles = ceil_div(plane, kBlockM);
   a.pair_tiles = (a.plane_tiles + 1) / 2;
   a.units = n * a.pair_tiles;
+  a.work = static_cast<long long>(a.units) * d;
   a.d_in = d + hist;
   a.d_out = d;
   a.hist = hist;
