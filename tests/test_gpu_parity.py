@@ -324,6 +324,28 @@ def test_head_small(n, d, h, w, cin, hist):
     assert float(out.abs().max()) <= 1.0
 
 
+@pytest.mark.parametrize("n,d,h,w,cin,hist", [
+    (3, 7, 24, 40, 64, 0),     # 12 tile pairs x 7 frames = 84 items: shares of 1-2 cross tile pairs
+    (2, 15, 16, 48, 64, 2),    # 6 x 15 = 90 items, carried history at every share start
+    (1, 16, 32, 80, 128, 0),   # 10 x 16 = 160 items, shares of 2-3 frames
+])
+def test_head_work_split_across_tile_pairs(n, d, h, w, cin, hist):
+    # more (tile pair, output frame) items than CTA pairs: shares start and
+    # end inside a tile pair's frames and re-read the frames before them.
+    # x has the head configuration's unit scale: at twice that scale the bf16
+    # g of the two-stage design alone (an fp64 model of its two roundings)
+    # puts the largest of ~10^5 outputs 0.017 off, above 2^-6 of the clamped
+    # maximum 1.0, whatever the kernel does.
+    g = torch.Generator(device=DEV).manual_seed(44)
+    x = torch.randn((n, d + hist, h, w, cin), generator=g, device=DEV).to(BF16)
+    wt = (torch.randn((12, cin, 3, 3, 3), generator=g, device=DEV) / (27 * cin) ** 0.5).to(BF16)
+    b = (torch.randn((12,), generator=g, device=DEV) * 0.3).to(BF16)
+    _, out, _ = run_head(x, wt, b, hist)
+    xn = to_np(x)
+    ref = oracle.head_out(xn[:, hist:], to_np(wt), to_np(b), history=xn[:, :2] if hist else None)
+    assert_parity(to_np(out), ref, f"head {n,d,h,w,cin,hist}")
+
+
 def test_head_stages_separately():
     inp = inputs.head_inputs(1, 2, 6, 9, 64, seed=42, device=DEV)
     wp = empty(3 * api.HEAD_G_CH * 64)
