@@ -1,6 +1,12 @@
-// Mid-block per-frame single-head attention, unfused:
-//   S = q k^T (tcgen05, fp32 out) -> P = softmax(scale * S) (bf16) -> O = P v
-// (tcgen05, v read as stored through an MN-major B operand, no transpose).
+// Mid-block per-frame single-head attention, two ways:
+//  - three passes: S = q k^T (tcgen05, fp32 out) -> P = softmax(scale * S)
+//    (bf16) -> O = P v (tcgen05, v read as stored through an MN-major B
+//    operand, no transpose);
+//  - through key-tile numerators: the scores kernel's epilogue turns each
+//    TMEM tile of S into E = exp2(kx*s - c_t) (bf16) and row statistics, a
+//    bandwidth pass moves every tile of a row onto the row's largest c_t by
+//    exact powers of two, and the PV epilogue divides each row by its sum --
+//    no fp32 S in memory and no softmax pass.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
