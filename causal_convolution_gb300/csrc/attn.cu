@@ -428,6 +428,7 @@ extern "C" cc_status cc_attn_pv_exp(const cc_bf16* e, const float* stats, const 
   a.out_batch = (long long)hw * ld_o;
   a.stats = const_cast<float2*>(reinterpret_cast<const float2*>(stats));
   a.stat_tiles = cc_attn_exp_key_tiles(hw);
+  a.batch_outer = 1;  // frame by frame: one frame's v (7 MB at C=1024) serves every concurrent tile
   return launch_tc_gemm_pair<256, kATiled3d, true, false, false, kEpiRowScale>(ta, tb, a, di,
                                                                               static_cast<cudaStream_t>(stream), what);
 }

@@ -45,6 +45,10 @@ struct GemmArgs {
   // one in-plane tile before moving on (temporal taps then hit L2).
   int frame_tiles;   // row tiles per frame (0 = plain order)
   int frames;        // frames (images x depth) when frame_tiles > 0
+  // Pair kernel: nonzero walks all row tiles of one batch before the next
+  // batch (the batch's B operand stays hot in L2); zero puts the batch
+  // inside the row tile (a row tile's A is shared by every batch at once).
+  int batch_outer;
   // im2col traversal: output grid and the bounding box's lower corner
   int img_w, img_h, img_d;
   int lo_w, lo_h, lo_d;

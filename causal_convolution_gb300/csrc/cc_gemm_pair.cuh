@@ -40,8 +40,14 @@ struct PairShape {
 __device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, int& batch, int& mp, int& nt) {
   nt = tile % a.n_tiles;
   const int r = tile / a.n_tiles;
-  batch = r % a.batches;
-  mp = r / a.batches;
+  if (a.batch_outer) {
+    const int mpt = (a.m_tiles + 1) / 2;
+    mp = r % mpt;
+    batch = r / mpt;
+  } else {
+    batch = r % a.batches;
+    mp = r / a.batches;
+  }
 }
 
 constexpr int kStoreChunk = 32;                          // fp32 columns per staged TMA store
