@@ -50,7 +50,7 @@ __device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, in
   }
 }
 
-constexpr int kStoreChunk = 32;                          // fp32 columns per staged TMA store
+constexpr int kStoreChunk = 32;  // fp32 columns per staged TMA store (64 bf16 columns in the exp-tile epilogue)
 constexpr int kStoreBufBytes = kBlockM * kStoreChunk * 4;  // 16 KB: 128 rows x 128 bytes
 
 template <int EPI>
