@@ -20,6 +20,8 @@ __all__ = [
     "cc_resample_prepare", "cc_resample_workspace_bytes", "cc_resample_phase_conv", "cc_resample_interleave",
     "cc_resample_up2", "cc_resample_up2_fused", "cc_resample_prepare_temporal",
     "cc_attn_ld", "cc_attn_workspace_bytes", "cc_attn_scores", "cc_attn_softmax", "cc_attn_pv", "cc_attn_frame",
+    "cc_attn_exp_key_tiles", "cc_attn_exp_workspace_bytes", "cc_attn_scores_exp", "cc_attn_exp_rescale",
+    "cc_attn_pv_exp", "cc_attn_frame_exp",
     "cc_head_prepare", "cc_head_workspace_bytes", "cc_head_temporal", "cc_head_stencil", "cc_head_out",
     "cc_head_out_noalloc", "HEAD_NOALLOC_SCRATCH_BYTES",
     "cc_debug_im2col_tile", "cc_debug_wait_timeout",

@@ -48,6 +48,14 @@ def test_python_binding_declares_every_symbol():
     assert set(declared_functions()) == set(_lib.SIGNATURES)
 
 
+def test_every_entry_point_has_an_exported_wrapper():
+    from causal_convolution_gb300 import api
+    # cc_last_error is read by the wrappers themselves (CCError messages)
+    missing = [n for n in declared_functions() if n != "cc_last_error" and n not in api.__all__]
+    assert not missing, missing
+    assert all(callable(getattr(api, n)) for n in api.__all__ if n.startswith("cc_"))
+
+
 def test_version_and_workspace_arithmetic(lib):
     assert lib.cc_version() >= 100
     assert lib.cc_resample_workspace_bytes(1, 8, 88, 156, 512) == 4 * 8 * 88 * 156 * 512 * 2
