@@ -50,8 +50,18 @@ KERNELS = ["conv3d_causal", "attn_scores_exp", "attn_exp_rescale", "attn_pv_exp"
 ROW_KERNELS = ["resample_phase_conv", "resample_interleave", "attn_scores", "attn_softmax", "attn_pv"]
 
 
+def real_taps(frames: int, taps_per_offset: int) -> int:
+    """Taps, summed over output frames 0..frames-1, that read a real input
+    frame when the two frames before frame 0 are zeros (temporal offsets 0, 1,
+    2 read frames t-2, t-1, t): frame 0 has one real offset, frame 1 two."""
+    return taps_per_offset * sum(min(3, t + 1) for t in range(frames))
+
+
 def algorithmic_work(rescale_bytes: float = 0.0):
     """Per-launch algorithmic work of every kernel: (bound, amount, unit).
+    The convolutions count the multiply-adds of taps that read a real input
+    frame: with zero history the products with the zero frames before frame
+    0 are exact zeros, which the GEMM skips per tile.
     rescale_bytes: what the rescale pass must move for the workload's inputs
     (it reads and writes only the key tiles not yet on their row's scale)."""
     cv = cc_inputs.CONFIGS["mid_conv"]
@@ -64,15 +74,15 @@ def algorithmic_work(rescale_bytes: float = 0.0):
     t, hw, c = at.d, at.hw, at.c
     ld = (hw + 7) // 8 * 8
     return {
-        "conv3d_causal": ("tensor", 2.0 * m_conv * cv.cout * 27 * cv.c, "flop"),
+        "conv3d_causal": ("tensor", 2.0 * (m_conv // cv.d) * cv.cout * real_taps(cv.d, 9) * cv.c, "flop"),
         "attn_scores": ("tensor", 2.0 * t * hw * hw * c, "flop"),
         "attn_softmax": ("hbm", t * hw * hw * 4.0 + t * hw * ld * 2.0, "byte"),
         "attn_pv": ("tensor", 2.0 * t * hw * hw * c, "flop"),
         "attn_scores_exp": ("tensor", 2.0 * t * hw * hw * c, "flop"),
         "attn_exp_rescale": ("hbm", rescale_bytes, "byte"),
         "attn_pv_exp": ("tensor", 2.0 * t * hw * hw * c, "flop"),
-        "resample_phase_conv": ("tensor", 2.0 * 4 * m_res * rs.cout * 12 * rs.c, "flop"),
-        "resample_up2_fused": ("tensor", 2.0 * 4 * m_res * rs.cout * 12 * rs.c, "flop"),
+        "resample_phase_conv": ("tensor", 2.0 * 4 * (m_res // rs.d) * rs.cout * real_taps(rs.d, 4) * rs.c, "flop"),
+        "resample_up2_fused": ("tensor", 2.0 * 4 * (m_res // rs.d) * rs.cout * real_taps(rs.d, 4) * rs.c, "flop"),
         "resample_interleave": ("hbm", (4 + 1 + 4) * m_res * rs.c * 2.0, "byte"),
         "head_temporal": ("hbm", m_head * hd.c * 2.0 + m_head * 112 * 2.0, "byte"),
         "head_stencil": ("hbm", m_head * 112 * 2.0 + m_head * 12 * 2.0, "byte"),
@@ -247,28 +257,37 @@ class Workload:
         api.cc_head_prepare(i["w"], self.head_wp)
         self.g = E(hd.n, hd.d, hd.h, hd.w, api.HEAD_G_CH)
         self.head_out = E(hd.n, hd.d, hd.h, hd.w, api.HEAD_COUT)
+
+        # a later chunk of a streamed decode: the causal stages get the previous
+        # chunk's last two input frames in front (hist = 2) instead of zeros
+        hf = cc_inputs.history_frames
+        self.conv_xh = torch.cat([hf(cv.n, cv.c, cv.h, cv.w, 101, device), self.conv_x], 1)
+        self.res_xh = torch.cat([hf(rs.n, rs.c, rs.h, rs.w, 102, device), self.res_x], 1)
+        self.head_xh = torch.cat([hf(hd.n, hd.c, hd.h, hd.w, 104, device), self.head_x], 1)
         torch.cuda.synchronize(device)
         api.cc_check_device()
 
-    def launches(self, stream):
-        """The hot path as (stage, launch) pairs in launch order, one per entry of KERNELS."""
+    def launches(self, stream, hist: int = 0):
+        """The hot path as (stage, launch) pairs in launch order, one per entry
+        of KERNELS; hist = 2 feeds the causal stages two carried history frames."""
         a = self.api
+        cx, rx, hx = (self.conv_xh, self.res_xh, self.head_xh) if hist else (self.conv_x, self.res_x, self.head_x)
         return (
-            ("conv", lambda: a.cc_conv3d_causal(self.conv_x, self.conv_wp, self.conv_b, self.conv_y, stream=stream)),
+            ("conv", lambda: a.cc_conv3d_causal(cx, self.conv_wp, self.conv_b, self.conv_y, hist=hist, stream=stream)),
             ("attn", lambda: a.cc_attn_scores_exp(self.q, self.k, self.e, self.st, self.scale, stream=stream)),
             ("attn", lambda: a.cc_attn_exp_rescale(self.e, self.st, self.at.hw, stream=stream)),
             ("attn", lambda: a.cc_attn_pv_exp(self.e, self.st, self.v, self.o, stream=stream)),
-            ("res", lambda: a.cc_resample_up2_fused(self.res_x, self.res_pw, self.res_b, self.res_skip,
-                                                    self.res_out, stream=stream)),
-            ("head", lambda: a.cc_head_temporal(self.head_x, self.head_wp, self.g, stream=stream)),
+            ("res", lambda: a.cc_resample_up2_fused(rx, self.res_pw, self.res_b, self.res_skip, self.res_out,
+                                                    hist=hist, stream=stream)),
+            ("head", lambda: a.cc_head_temporal(hx, self.head_wp, self.g, hist=hist, stream=stream)),
             ("head", lambda: a.cc_head_stencil(self.g, self.head_b, self.head_out, stream=stream)),
         )
 
-    def step(self, stream, ev=None):
+    def step(self, stream, ev=None, hist: int = 0):
         """The whole hot path once. With `ev` (len(KERNELS)+1 events) each launch is bracketed."""
         if ev is not None:
             ev[0].record(stream)
-        for j, (_, launch) in enumerate(self.launches(stream)):
+        for j, (_, launch) in enumerate(self.launches(stream, hist)):
             launch()
             if ev is not None:
                 ev[j + 1].record(stream)
@@ -579,6 +598,20 @@ def main(argv=None):
                   for j, name in enumerate(KERNELS)}
     ms_step = max_over_ranks(elapsed / args.steps, device)
 
+    # steady state: the same step on a later chunk of a streamed decode (two
+    # carried history frames, so no zero-padding taps to skip), outside the
+    # timed region of `value`
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        wl.step(stream, hist=2)
+    for k in range(args.steps):
+        wl.step(stream, sev[k], hist=2)
+    torch.cuda.synchronize(device)
+    steady = {name: float(np.mean([sev[k][j].elapsed_time(sev[k][j + 1]) for k in range(args.steps)]))
+              for j, name in enumerate(KERNELS)}
+    steady_ms = float(np.mean([sev[k][0].elapsed_time(sev[k][-1]) for k in range(args.steps)]))
+    wl.api.cc_check_device()
+
     # the resampler's two-pass form (rows a4, a5), outside the step
     rev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROW_KERNELS) + 1)] for _ in range(args.steps)]
     for _ in range(2):
@@ -652,6 +685,11 @@ def main(argv=None):
         "traffic_source": "profiles/ncu_traffic.json (per-launch dram read+write of one ncu capture; null when the "
                           "kernel's sources changed since)",
         "roofline": roofline,
+        "steady_state": {"ms_per_step": round(steady_ms, 4),
+                         "what": "the same step on a later chunk of a streamed decode: conv, resampler and head get "
+                                 "the previous chunk's last two input frames (hist=2) instead of the zero frames, so "
+                                 "no tap can be skipped",
+                         "kernels_ms": {n: round(v, 4) for n, v in steady.items()}},
         "e2e": {"value": round(e2e_ms / ws, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": len(KERNELS) * args.steps,
         "clocks": clocks.summary(),

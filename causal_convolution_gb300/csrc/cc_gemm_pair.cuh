@@ -50,6 +50,37 @@ __device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, in
   }
 }
 
+// Taps are ordered by their temporal offset. With zero frames before frame 0
+// (lo_d < 0), a tap whose input frame t + od + lo_d is negative for every row
+// of the pair tile multiplies only the causal zero padding: its exact-zero
+// products are skipped, and the tile's k-loop starts at the first tap that
+// reads a real frame for some row. The last tap (od = -lo_d) always does.
+template <int AMODE>
+__device__ __forceinline__ int tile_first_tap(const GemmArgs& a, int batch, int mp) {
+  if (AMODE != kAIm2col || a.lo_d >= 0) return 0;
+  const long long plane = static_cast<long long>(a.img_h) * a.img_w;
+  const long long per_image = plane * a.img_d;
+  const long long m0 = static_cast<long long>(mp) * 2 * kBlockM;
+  const long long m1 = min(m0 + 2 * kBlockM, static_cast<long long>(a.m_total)) - 1;
+  // the latest frame any row of the tile lies in (a tile across an image
+  // boundary holds the previous image's last frame)
+  const int t_max = m0 / per_image != m1 / per_image ? a.img_d - 1 : static_cast<int>((m1 / plane) % a.img_d);
+  int tap = 0;
+  while (tap < a.taps - 1 && t_max + ((a.tap_off[batch * a.taps + tap] >> 16) & 0xff) + a.lo_d < 0) ++tap;
+  return tap;
+}
+
+// The k-th tile of a CTA pair: waves of npairs consecutive tiles, walked
+// forward in even waves and backward in odd ones, so a pair that gets a
+// short tile (leading zero taps skipped) early gets a long one next. -1 when
+// the pair has no tile in that (last, partial) wave; num_tiles when done.
+__device__ __forceinline__ int pair_tile(const GemmArgs& a, int pair, int npairs, int k) {
+  const int base = k * npairs;
+  if (base >= a.num_tiles) return a.num_tiles;
+  const int tile = (k & 1) ? base + npairs - 1 - pair : base + pair;
+  return tile < a.num_tiles ? tile : -1;
+}
+
 constexpr int kStoreChunk = 32;  // fp32 columns per staged TMA store (64 bf16 columns in the exp-tile epilogue)
 constexpr int kStoreBufBytes = kBlockM * kStoreChunk * 4;  // 16 KB: 128 rows x 128 bytes
 
@@ -115,7 +146,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
+      for (int k = 0, tile; ok && (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
+        if (tile < 0) continue;
         int batch, mp, nt;
         pair_decode_tile(args, tile, batch, mp, nt);
         const int m0 = (2 * mp + static_cast<int>(rank)) * kBlockM;
@@ -133,7 +165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           ch += args.lo_h;
           cd += args.lo_d;
         }
-        for (int tap = 0; ok && tap < args.taps; ++tap) {
+        for (int tap = tile_first_tap<AMODE>(args, batch, mp); ok && tap < args.taps; ++tap) {
           const int off = (AMODE == kAIm2col) ? args.tap_off[batch * args.taps + tap] : 0;
           const int brow = batch * args.b_rows_per_batch + tap * args.b_rows_per_tap + nb0;
           for (int kb = 0; kb < args.kb_per_tap; ++kb) {
@@ -187,14 +219,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // 8-row groups are 1024 bytes apart; MN-major 64-column blocks 8192 bytes
       const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, 1024);
       const uint64_t b_desc0 = B_MN ? sdesc_sw128(smem_u32(sB), 8192, 1024) : sdesc_sw128(smem_u32(sB), 16, 1024);
-      for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
+      for (int k = 0, tile; ok && (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
+        if (tile < 0) continue;
+        int batch, mp, nt;
+        pair_decode_tile(args, tile, batch, mp, nt);
+        const int kb0 = tile_first_tap<AMODE>(args, batch, mp) * args.kb_per_tap;
         if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, args.err, tlim)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * S::kAccCols;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kblocks; ++kb) {
           if (!mbar_wait(smem_u32(&full[stage]), phase, args.err, tlim)) {
             ok = false;
             break;
@@ -208,7 +244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (S::kBBytes >> 4);
 #pragma unroll
           for (int k = 0; k < kBlockK / kUmmaK; ++k)
-            mma_bf16_pair(d_tmem, ad + 2 * k, bd + (B_MN ? 128 : 2) * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            mma_bf16_pair(d_tmem, ad + 2 * k, bd + (B_MN ? 128 : 2) * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           mma_commit_pair_both(smem_u32(&empty[stage]));
           if (++stage == STAGES) {
             stage = 0;
@@ -238,7 +274,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int chunk = 0;
-    for (int tile = pair; tile < args.num_tiles; tile += npairs) {
+    for (int k = 0, tile; (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
+      if (tile < 0) continue;
       int batch, mp, nt;
       pair_decode_tile(args, tile, batch, mp, nt);
       if (!named_barrier_and(1, 128, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
@@ -333,7 +370,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int chunk = 0;
-    for (int tile = pair; tile < args.num_tiles; tile += npairs) {
+    for (int k = 0, tile; (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
+      if (tile < 0) continue;
       int batch, mp, nt;
       pair_decode_tile(args, tile, batch, mp, nt);
       // uniform over the four epilogue warps (shared named barriers below)
@@ -379,7 +417,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = pair; tile < args.num_tiles; tile += npairs) {
+    for (int k = 0, tile; (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
+      if (tile < 0) continue;
       int batch, mp, nt;
       pair_decode_tile(args, tile, batch, mp, nt);
       // warp-uniform: the lanes leave together (they share .sync.aligned ops)

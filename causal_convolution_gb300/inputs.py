@@ -80,6 +80,12 @@ def conv_inputs(n, d, h, w, cin, cout, seed, bias_var=0.02, device="cpu", histor
     return out
 
 
+def history_frames(n, c, h, w, seed, device="cpu"):
+    """Two N(0,1) frames [N, 2, H, W, C] bf16 to carry in front of a chunk's
+    input (the previous chunk's last two frames in a streamed decode)."""
+    return _act(_gen(seed, device), n, c, 2, h, w, device)
+
+
 def resample_inputs(n, d, hl, wl, c, seed, bias_var=0.02, device="cpu"):
     """x [N,D,HL,WL,C], weight [C,C,3,3,3], bias [C], skip [N,D,HL,WL,C]."""
     g = _gen(seed, device)

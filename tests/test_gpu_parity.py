@@ -114,6 +114,20 @@ def test_conv3d_causal_small(n, d, h, w, cin, cout, hist, bias):
     assert_parity(to_np(y), ref, f"conv {n,d,h,w,cin,cout,hist}")
 
 
+@pytest.mark.parametrize("n,d,h,w", [
+    (2, 3, 8, 20),    # 480 rows per image: 256-row pair tiles straddle frames and the image boundary
+    (1, 5, 16, 16),   # 256 rows per frame: every pair tile inside one frame
+    (3, 2, 5, 7),     # 70 rows per image: every pair tile spans several images
+])
+def test_conv3d_zero_history_taps_skipped_per_tile(n, d, h, w):
+    # with zero history a pair tile skips the leading taps that read only the
+    # zero frames before frame 0 for all of its rows; the result must not
+    # change, whatever frames and images the tile spans
+    inp, _, y = run_conv(n, d, h, w, 64, 64, 0)
+    ref = oracle.causal_conv3d(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"]))
+    assert_parity(to_np(y), ref, f"conv {n,d,h,w}")
+
+
 def test_conv3d_mid_block_config_sampled():
     c = inputs.CONFIGS["mid_conv"]
     inp = inputs.make_config_inputs("mid_conv", device=DEV)
@@ -449,6 +463,23 @@ def test_resample_fused_small(n, d, hl, wl, cin, cout, hist):
     xn = to_np(x)
     ref = oracle.resample_up2(xn[:, hist:], to_np(w), to_np(b), to_np(s), history=xn[:, :2] if hist else None)
     assert_parity(to_np(out), ref, f"fused resampler {n,d,hl,wl,cin,cout,hist}")
+
+
+@pytest.mark.parametrize("n,d,hl,wl,temporal", [(2, 3, 8, 20, False), (1, 5, 16, 16, False), (2, 3, 8, 20, True)])
+def test_resample_fused_zero_history_taps_skipped_per_tile(n, d, hl, wl, temporal):
+    g = torch.Generator(device=DEV).manual_seed(29)
+    cin = cout = 64
+    x = torch.randn((n, d, hl, wl, cin), generator=g, device=DEV).to(BF16)
+    w = (torch.randn((cout, cin, 3, 3, 3), generator=g, device=DEV) / (27 * cin) ** 0.5).to(BF16)
+    b = (torch.randn((cout,), generator=g, device=DEV) * 0.1).to(BF16)
+    s = torch.randn((n, d, hl, wl, cout), generator=g, device=DEV).to(BF16)
+    pw = empty((64 if temporal else 48) * cout * cin)
+    (api.cc_resample_prepare_temporal if temporal else api.cc_resample_prepare)(w, pw)
+    out = empty(n, 2 * d if temporal else d, 2 * hl, 2 * wl, cout)
+    api.cc_resample_up2_fused(x, pw, b, s, out, temporal=temporal)
+    api.cc_check_device()
+    ref = oracle.resample_up2(to_np(x), to_np(w), to_np(b), to_np(s), temporal=temporal)
+    assert_parity(to_np(out), ref, f"fused resampler {n,d,hl,wl,temporal}")
 
 
 def test_resample_fused_matches_two_pass():
