@@ -42,7 +42,7 @@
  *  [HEAD] FastVideo wan22_vae_decode solution/head.cu -- header comment
  *         (conv_out folded into a 3x1x1 conv with 9x12 output channels, then
  *         a 3x3 stencil, bias and clamp) and head_stencil_kernel.
- *  [TASK] the stack's definition: causal 3x3x3 conv with two history frames,
+ *  [STACK] the stack's definition: causal 3x3x3 conv with two history frames,
  *         zeros before frame 0, spatial zero padding 1, fp32 accumulation.
  */
 #ifndef CC_H_
@@ -76,7 +76,7 @@ int cc_version(void);
  * word. Returns CC_OK, CC_ERR_TIMEOUT, CC_ERR_DEVICE or CC_ERR_CUDA. */
 cc_status cc_check_device(void* stream);
 
-/* ------------------------------------------------ causal 3x3x3 conv [TASK] */
+/* ------------------------------------------------ causal 3x3x3 conv [STACK] */
 
 /* Repacks w [C_out, C_in, 3, 3, 3] into wp [27][C_out][C_in] (tap-major,
  * tap = kt*9 + kh*3 + kw, each row K-major), the B operand of the implicit

@@ -24,8 +24,9 @@ Sources (pages of the reference material, by title and item):
   ``head_stencil_kernel``: conv_out to 12 channels, bias, clamp to [-1, 1],
   zero padding in the plane; the two-stage split (temporal 3x1x1 conv into
   9x12 channels, then a 3x3 spatial sum) is the same sum regrouped.
-* The benchmark spec of this stack: causal 3x3x3 convolution with two history
-  frames (zeros before frame 0) and spatial zero padding of 1.
+* The stack's definition: a causal 3x3x3 convolution with two history frames
+  (zeros before frame 0 of a first chunk) and spatial zero padding of 1, the
+  history frames and padding the ``resample_upsample`` comment also names.
 
 Readings where the pages are silent (each one is listed with its reason in the
 design notes of the repository):
