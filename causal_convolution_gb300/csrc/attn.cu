@@ -287,6 +287,10 @@ __global__ void __launch_bounds__(kRescaleWarps * 32) exp_rescale_kernel(__nv_bf
                                                                           float2* __restrict__ stats,
                                                                           long long rows, int hw, long long ld_e,
                                                                           int tiles) {
+  // launched after the scores kernel that writes e and stats; many blocks per
+  // SM, so it does not let the next kernel in early (its CTAs would take SMs
+  // this grid's later blocks still need)
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * kRescaleWarps + warp;
   if (row >= rows) return;
@@ -392,9 +396,11 @@ extern "C" cc_status cc_attn_exp_rescale(cc_bf16* e, float* stats, int t, int hw
   if ((st = device_info(&di)) != CC_OK) return st;
   const long long rows = (long long)t * hw;
   const unsigned grid = (unsigned)((rows + kRescaleWarps - 1) / kRescaleWarps);
-  exp_rescale_kernel<<<grid, kRescaleWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<__nv_bfloat16*>(e), reinterpret_cast<float2*>(stats), rows, hw, ld_e,
-      cc_attn_exp_key_tiles(hw));
+  const cudaError_t err = launch_pdl(exp_rescale_kernel, dim3(grid), dim3(kRescaleWarps * 32), 0,
+                                     static_cast<cudaStream_t>(stream), reinterpret_cast<__nv_bfloat16*>(e),
+                                     reinterpret_cast<float2*>(stats), rows, hw, (long long)ld_e,
+                                     cc_attn_exp_key_tiles(hw));
+  if (err != cudaSuccess) return fail(CC_ERR_CUDA, "%s: launch: %s", what, cudaGetErrorString(err));
   return launch_status(what);
 }
 

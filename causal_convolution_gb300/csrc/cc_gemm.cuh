@@ -262,6 +262,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set up: let the next kernel on the stream be scheduled, then wait for the
+  // previous one before the first global access
+  pdl_launch_dependents();
+  pdl_wait();
   const uint64_t tlim = args.timeout_ns;
 
   if (warp == 0) {

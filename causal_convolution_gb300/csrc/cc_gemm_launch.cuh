@@ -20,7 +20,8 @@ cc_status launch_tc_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs&
   args.err = di.err_word;
   args.timeout_ns = kWaitLimitNs;
   const int grid = std::min(args.num_tiles, di.sm_count);
-  kern<<<grid, kGemmThreads, S::kSmemBytes, stream>>>(ta, tb, args);
+  e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), S::kSmemBytes, stream, ta, tb, args);
+  if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: launch: %s", what, cudaGetErrorString(e));
   return launch_status(what);
 }
 
@@ -40,7 +41,8 @@ cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, Gemm
   args.err = di.err_word;
   args.timeout_ns = kWaitLimitNs;
   const int pairs = std::min(args.num_tiles, di.sm_count / 2);
-  kern<<<2 * pairs, kGemmThreads, S::kSmemBytes, stream>>>(ta, tb, tc ? *tc : tb, args);
+  e = launch_pdl(kern, dim3(2 * pairs), dim3(kGemmThreads), S::kSmemBytes, stream, ta, tb, tc ? *tc : tb, args);
+  if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: launch: %s", what, cudaGetErrorString(e));
   return launch_status(what);
 }
 

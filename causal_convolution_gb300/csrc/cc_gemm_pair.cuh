@@ -138,6 +138,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set up: let the next kernel on the stream be scheduled, then wait for the
+  // previous one before the first global access
+  pdl_launch_dependents();
+  pdl_wait();
   const uint64_t tlim = args.timeout_ns;
 
   if (warp == 0) {

@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "cc.h"
 
@@ -19,6 +20,27 @@ namespace cc {
 cc_status fail(cc_status st, const char* fmt, ...);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel on the stream is still finishing (its CTAs take
+// SMs as that kernel's CTAs exit), do its setup, and then block in
+// griddepcontrol.wait until the previous kernel has completed and its writes
+// are visible -- the same ordering as a plain launch, with the setup hidden.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Per-device facts, cached on first use.
 struct DeviceInfo {

@@ -74,6 +74,16 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Programmatic dependent launch. launch_dependents lets the next kernel on the
+// stream be scheduled (persistent kernels call it at the start: the next
+// kernel's CTAs still need the SMs this one frees); wait blocks until every
+// kernel this one depends on has completed and its memory is visible, and is
+// a no-op for a kernel launched without programmatic serialization.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA --
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -138,6 +138,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set up: let the next kernel on the stream be scheduled, then wait for the
+  // previous one before the first global access
+  pdl_launch_dependents();
+  pdl_wait();
   const uint64_t tlim = a.timeout_ns;
 
   if (warp == 0) {
@@ -358,8 +362,9 @@ cc_status launch_head_temporal(const CUtensorMap& tx, const CUtensorMap& tw, Hea
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "head_temporal: shared-memory attribute: %s", cudaGetErrorString(e));
   a.err = di.err_word;
   a.timeout_ns = kWaitLimitNs;
-  kern<<<2 * static_cast<int>(std::min<long long>(a.work, di.sm_count / 2)), kGemmThreads, S::kSmemBytes, stream>>>(
-      tx, tw, a);
+  e = launch_pdl(kern, dim3(2 * static_cast<int>(std::min<long long>(a.work, di.sm_count / 2))), dim3(kGemmThreads),
+                 S::kSmemBytes, stream, tx, tw, a);
+  if (e != cudaSuccess) return fail(CC_ERR_CUDA, "head_temporal: launch: %s", cudaGetErrorString(e));
   return launch_status("head_temporal");
 }
 

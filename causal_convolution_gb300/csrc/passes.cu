@@ -128,6 +128,10 @@ __global__ void __launch_bounds__(kStThreads, 1)
     tma_prefetch_map(&tmG);
   }
   __syncthreads();
+  // set up: let the next kernel on the stream be scheduled, then wait for the
+  // previous one before the first global access
+  pdl_launch_dependents();
+  pdl_wait();
 
   auto issue = [&](int t, int s) {
     int frame, hb, wb;
@@ -285,7 +289,9 @@ extern "C" cc_status cc_head_stencil(const cc_bf16* g, const cc_bf16* bias, cc_b
   a.timeout_ns = kWaitLimitNs;
   cudaError_t e = cudaFuncSetAttribute(head_stencil_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStSmem);
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: shared-memory attribute: %s", what, cudaGetErrorString(e));
-  head_stencil_kernel<<<std::min(a.tiles, di.sm_count), kStThreads, kStSmem, static_cast<cudaStream_t>(stream)>>>(tm, a);
+  e = launch_pdl(head_stencil_kernel, dim3(std::min(a.tiles, di.sm_count)), dim3(kStThreads), kStSmem,
+                 static_cast<cudaStream_t>(stream), tm, a);
+  if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: launch: %s", what, cudaGetErrorString(e));
   return launch_status(what);
 }
 
