@@ -604,3 +604,51 @@ def test_resample_chunked_streaming_equals_one_call(temporal):
                               hist=2, temporal=temporal)
     api.cc_check_device()
     assert torch.equal(torch.cat([y0, y1], 1), full)
+
+
+# ------------------------------------- dependent launches on one stream --
+
+def test_dependent_chain_on_one_stream_matches_synchronised_run():
+    # conv -> fused resampler -> head, each reading the previous output, queued
+    # back to back on one stream (the kernels are launched with programmatic
+    # serialization and wait for their predecessor before the first global
+    # access); the result must equal, bit for bit, the same launches with the
+    # host synchronising after each
+    g = torch.Generator(device=DEV).manual_seed(71)
+    n, d, h, w, c = 1, 3, 24, 40, 64
+    x = torch.randn((n, d, h, w, c), generator=g, device=DEV).to(BF16)
+    wc = (torch.randn((c, c, 3, 3, 3), generator=g, device=DEV) / (27 * c) ** 0.5).to(BF16)
+    bc = (torch.randn((c,), generator=g, device=DEV) * 0.1).to(BF16)
+    wr = (torch.randn((c, c, 3, 3, 3), generator=g, device=DEV) / (27 * c) ** 0.5).to(BF16)
+    br = (torch.randn((c,), generator=g, device=DEV) * 0.1).to(BF16)
+    wh = (torch.randn((12, c, 3, 3, 3), generator=g, device=DEV) / (27 * c) ** 0.5).to(BF16)
+    bh = (torch.randn((12,), generator=g, device=DEV) * 0.1).to(BF16)
+    wpc = empty(27 * c * c)
+    api.cc_conv3d_prepare(wc, wpc)
+    pw = empty(48 * c * c)
+    api.cc_resample_prepare(wr, pw)
+    wph = empty(3 * api.HEAD_G_CH * c)
+    api.cc_head_prepare(wh, wph)
+    torch.cuda.synchronize()
+
+    def chain(sync):
+        y = empty(n, d, h, w, c)
+        up = empty(n, d, 2 * h, 2 * w, c)
+        out = empty(n, d, 2 * h, 2 * w, api.HEAD_COUT)
+        ws = torch.empty(api.cc_head_workspace_bytes(n, d, 2 * h, 2 * w), dtype=torch.uint8, device=DEV)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            api.cc_conv3d_causal(x, wpc, bc, y, stream=s)
+            if sync:
+                s.synchronize()
+            api.cc_resample_up2_fused(y, pw, br, y, up, stream=s)
+            if sync:
+                s.synchronize()
+            api.cc_head_out(up, wph, bh, out, ws, stream=s)
+        s.synchronize()
+        api.cc_check_device()
+        return y, up, out
+
+    a, b = chain(False), chain(True)
+    for name, u, v in zip(("conv", "resampler", "head"), a, b):
+        assert torch.equal(u, v), f"{name}: the queued chain differs from the synchronised one"
