@@ -596,6 +596,10 @@ def main(argv=None):
     elapsed = t_start.elapsed_time(t_end)
     per_kernel = {name: float(np.mean([evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)]))
                   for j, name in enumerate(KERNELS)}
+    step_times = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
+    per_kernel_stats = {name: (float(np.median([evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)])),
+                               float(np.min([evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)])))
+                        for j, name in enumerate(KERNELS)}
     ms_step = max_over_ranks(elapsed / args.steps, device)
 
     # steady state: the same step on a later chunk of a streamed decode (two
@@ -656,6 +660,10 @@ def main(argv=None):
     traffic = measured_traffic()
     for name in roofs:
         roofs[name]["traffic"] = traffic.get(name)  # per-launch DRAM bytes from ncu, None if stale
+        if traffic.get(name):  # the same launch's DRAM bytes over its time, GB/s
+            roofs[name]["traffic_gbs"] = traffic[name] / (per_kernel[name] * 1e-3) / 1e9
+        if name in per_kernel_stats:
+            roofs[name]["ms_median"], roofs[name]["ms_min"] = per_kernel_stats[name]
     dominant = max(KERNELS, key=lambda n: per_kernel[n])
     dr = roofs[dominant]
     roofline = {"bound": dr["bound"], "achieved": round(dr["achieved"], 2), "peak": dr["peak"], "unit": dr["unit"],
@@ -666,6 +674,8 @@ def main(argv=None):
         "metric": METRIC, "value": round(ms_step / ws, 4), "unit": "ms", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal inputs, fan-in-scaled weights)",
+        "step_ms_stats": {"mean": round(float(np.mean(step_times)), 4), "median": round(float(np.median(step_times)), 4),
+                          "min": round(float(np.min(step_times)), 4)},
         "config": config_dict(ws),
         "conv_tflops": round(roofs["conv3d_causal"]["achieved"], 2),
         "conv_frac_of_bf16_peak": round(roofs["conv3d_causal"]["frac"], 4),
