@@ -41,7 +41,8 @@ def scaled_inputs(t, hw, c, seed, gain):
 
 
 @pytest.mark.parametrize("t,hw,c", [(2, 200, 64), (1, 130, 128), (3, 64, 64), (1, 1, 64), (2, 333, 1024),
-                                    (1, 256, 64), (1, 257, 64), (1, 512, 128), (2, 700, 128), (1, 4200, 64)])
+                                    (1, 256, 64), (1, 257, 64), (1, 512, 128), (2, 700, 128), (1, 4200, 64),
+                                    (5, 8, 64), (1, 129, 192)])
 def test_attn_exp_small(t, hw, c):
     inp = inputs.attn_inputs(t, hw, c, seed=41, device=DEV)
     o = run_exp(inp["q"], inp["k"], inp["v"])

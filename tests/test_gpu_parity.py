@@ -106,6 +106,9 @@ def test_conv3d_prepare_is_a_pure_repack():
     (1, 3, 4, 7, 64, 32, 2, True),       # carried history frames
     (1, 2, 3, 5, 192, 64, 0, False),     # no bias
     (1, 1, 1, 1, 64, 16, 0, True),       # a single position
+    (1, 3, 1, 200, 64, 64, 0, True),     # one-row planes: every tap row above and below is padding
+    (1, 3, 200, 1, 64, 64, 0, True),     # one-column planes
+    (1, 1, 6, 9, 1024, 16, 2, True),     # one frame after two carried frames; K = 27,648, N = 16
 ])
 def test_conv3d_causal_small(n, d, h, w, cin, cout, hist, bias):
     inp, _, y = run_conv(n, d, h, w, cin, cout, hist, with_bias=bias)
@@ -452,6 +455,8 @@ def test_resample_fused_toy_config_full():
     (2, 2, 3, 4, 128, 64, 2),
     (1, 2, 9, 13, 64, 272, 0),
     (1, 1, 1, 1, 64, 16, 0),     # a single low-resolution pixel (single-CTA path)
+    (1, 2, 1, 150, 64, 64, 0),   # one-row low-resolution planes
+    (1, 1, 12, 11, 128, 16, 2),  # one frame after two carried frames, N = 16
 ])
 def test_resample_fused_small(n, d, hl, wl, cin, cout, hist):
     g = torch.Generator(device=DEV).manual_seed(22)
