@@ -1,0 +1,38 @@
+"""Host-side arithmetic of the bench line and the seeded inputs (CPU only)."""
+
+import torch
+
+import bench
+from causal_convolution_gb300 import inputs
+
+
+def test_real_taps_counts_the_taps_that_read_a_real_frame():
+    # temporal offsets 0, 1, 2 read frames t-2, t-1, t; frames before 0 are zeros
+    assert bench.real_taps(1, 9) == 9
+    assert bench.real_taps(2, 9) == 9 + 18
+    assert bench.real_taps(4, 9) == 9 + 18 + 27 + 27
+    brute = sum(sum(1 for kt in range(3) if t + kt - 2 >= 0) for t in range(8)) * 4
+    assert bench.real_taps(8, 4) == brute == 84
+
+
+def test_algorithmic_work_of_the_convolutions():
+    work = bench.algorithmic_work(rescale_bytes=123.0)
+    cv, rs = inputs.CONFIGS["mid_conv"], inputs.CONFIGS["resampler"]
+    plane = cv.h * cv.w
+    # 4 frames: 9 + 18 + 27 + 27 taps of 1024 x 1024 multiply-adds per position
+    assert work["conv3d_causal"] == ("tensor", 2.0 * plane * 1024 * 1024 * 81, "flop")
+    assert abs(work["conv3d_causal"][1] / 0.583e12 - 1) < 1e-3
+    # the resampler: 4 phases x 4 spatial taps x (1 + 2 + 3 x 6) temporal taps per low-res position
+    low = rs.h * rs.w
+    assert work["resample_up2_fused"][1] == 2.0 * 4 * low * 512 * 512 * 4 * 21
+    assert work["resample_up2_fused"] == work["resample_phase_conv"]
+    assert work["attn_exp_rescale"] == ("hbm", 123.0, "byte")
+    assert work["attn_scores_exp"] == work["attn_scores"] == work["attn_pv_exp"]
+
+
+def test_history_frames_are_seeded_and_shaped():
+    a = inputs.history_frames(1, 64, 3, 5, seed=7)
+    b = inputs.history_frames(1, 64, 3, 5, seed=7)
+    c = inputs.history_frames(1, 64, 3, 5, seed=8)
+    assert a.shape == (1, 2, 3, 5, 64) and a.dtype == torch.bfloat16 and a.is_contiguous()
+    assert torch.equal(a, b) and not torch.equal(a, c)
