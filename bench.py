@@ -402,6 +402,12 @@ class Workload:
 
 # -------------------------------------------------------------- CPU oracle --
 
+# outputs per oracle call for conv, attention, resampler, head: large enough
+# that each call's setup (the conv widens and slices 27 weight taps of 8 MB
+# per call) is a small part of its time
+ORACLE_BATCH = (512, 1024, 2048, 8192)
+
+
 def oracle_sample_step(cpu, budget_s: float, rng):
     """Times the fp64 oracle on a bounded sample of each stage's outputs and
     extrapolates by output count to ms per chunk. Returns (ms_per_chunk,
@@ -413,18 +419,18 @@ def oracle_sample_step(cpu, budget_s: float, rng):
     desc = []
     per_stage = budget_s / 4.0
 
-    def timed(fn, total):
-        """Batches of sampled outputs (8 to 4096 per call) until the stage's
-        share of the budget is spent; returns (points, seconds, ms per chunk)."""
-        npts, dt, n = 0, 0.0, 8
-        while True:
+    def timed(fn, total, batch):
+        """Calls of `batch` sampled outputs until the stage's share of the
+        budget is spent (at least one); returns (points, seconds, ms per
+        chunk). The batch is fixed per stage, so the per-call setup is spread
+        over the same number of outputs whatever the budget."""
+        npts, dt = 0, 0.0
+        while npts == 0 or dt < per_stage:
             t0 = time.perf_counter()
-            fn(n)
+            fn(batch)
             dt += time.perf_counter() - t0
-            npts += n
-            if dt >= per_stage:
-                return npts, dt, dt * total / npts * 1e3
-            n = int(min(4096, max(8, (per_stage - dt) * npts / dt)))
+            npts += batch
+        return npts, dt, dt / npts * total * 1e3
 
     stages = []
     cv = cc_inputs.CONFIGS["mid_conv"]
@@ -444,11 +450,11 @@ def oracle_sample_step(cpu, budget_s: float, rng):
     stages.append(("head", hd.n * hd.d * hd.h * hd.w,
                    lambda P: oracle.head_out_at(cpu["head_x"], cpu["head_w"], cpu["head_b"],
                                                 _pts(rng, P, hd.n, hf, hd.h, hd.w))))
-    for name, total, fn in stages:
-        npts, dt, ms = timed(fn, total)
+    for (name, total, fn), batch in zip(stages, ORACLE_BATCH):
+        npts, dt, ms = timed(fn, total, batch)
         spent += dt
         total_ms += ms
-        desc.append(f"{name}: {npts} of {total} outputs")
+        desc.append(f"{name}: {npts} of {total} outputs in batches of {batch}")
     return total_ms, spent, "; ".join(desc) + " (extrapolated by output count)"
 
 
@@ -457,9 +463,10 @@ def _pts(rng, p, n, d, h, w):
 
 
 def host_inputs(device, head_frames=3):
-    """The oracle's inputs on the host (the head keeps its first frames only:
-    sampled outputs there need frames t-2..t, all held)."""
-    f = lambda t: t.float().cpu().numpy()
+    """The oracle's inputs on the host, already float64 (the oracle widens its
+    inputs on every call otherwise); the head keeps its first frames only:
+    sampled outputs there need frames t-2..t, all held."""
+    f = lambda t: t.double().cpu().numpy()
     out = {}
     i = cc_inputs.make_config_inputs("mid_conv", device)
     out.update(conv_x=f(i["x"]), conv_w=f(i["w"]), conv_b=f(i["b"]))
