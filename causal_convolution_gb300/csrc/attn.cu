@@ -149,6 +149,7 @@ extern "C" cc_status cc_attn_scores(const cc_bf16* q, const cc_bf16* k, float* s
                                     int64_t ld_k, int64_t ld_s, void* stream) {
   const char* what = "attn_scores";
   cc_status st;
+  if (empty_request(what, {t, hw}, &st)) return st;
   if ((st = check_ptr(what, q)) != CC_OK || (st = check_ptr(what, k)) != CC_OK || (st = check_ptr(what, s)) != CC_OK)
     return st;
   if (t <= 0 || hw <= 0 || c <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
@@ -190,6 +191,7 @@ extern "C" cc_status cc_attn_softmax(const float* s, cc_bf16* p, int t, int hw, 
                                      float scale, void* stream) {
   const char* what = "attn_softmax";
   cc_status st;
+  if (empty_request(what, {t, hw}, &st)) return st;
   if ((st = check_ptr(what, s)) != CC_OK || (st = check_ptr(what, p)) != CC_OK) return st;
   if (t <= 0 || hw <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
   if (ld_s < hw || ld_p < hw || ld_s % 4 || ld_p % 8)
@@ -221,6 +223,7 @@ extern "C" cc_status cc_attn_pv(const cc_bf16* p, const cc_bf16* v, cc_bf16* o, 
                                 int64_t ld_v, int64_t ld_o, void* stream) {
   const char* what = "attn_pv";
   cc_status st;
+  if (empty_request(what, {t, hw}, &st)) return st;
   if ((st = check_ptr(what, p)) != CC_OK || (st = check_ptr(what, v)) != CC_OK || (st = check_ptr(what, o)) != CC_OK)
     return st;
   if (t <= 0 || hw <= 0 || c <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
@@ -255,9 +258,9 @@ extern "C" cc_status cc_attn_frame(const cc_bf16* q, const cc_bf16* k, const cc_
                                    int c, int64_t ld_q, int64_t ld_k, int64_t ld_v, int64_t ld_o, float scale,
                                    void* ws, size_t ws_bytes, void* stream) {
   const char* what = "attn_frame";
-  if (t <= 0 || hw <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
-  cc_status st = check_ptr(what, ws);
-  if (st != CC_OK) return st;
+  cc_status st;
+  if (empty_request(what, {t, hw}, &st)) return st;
+  if ((st = check_ptr(what, ws)) != CC_OK) return st;
   const size_t need = cc_attn_workspace_bytes(t, hw);
   if (ws_bytes < need) return fail(CC_ERR_INVALID, "%s: workspace of %zu bytes, need %zu", what, ws_bytes, need);
   const int64_t ld = cc_attn_ld(hw);
@@ -352,6 +355,7 @@ extern "C" cc_status cc_attn_scores_exp(const cc_bf16* q, const cc_bf16* k, cc_b
                                         int c, int64_t ld_q, int64_t ld_k, int64_t ld_e, float scale, void* stream) {
   const char* what = "attn_scores_exp";
   cc_status st;
+  if (empty_request(what, {t, hw}, &st)) return st;
   if ((st = check_ptr(what, q)) != CC_OK || (st = check_ptr(what, k)) != CC_OK || (st = check_ptr(what, e)) != CC_OK ||
       (st = check_ptr(what, stats)) != CC_OK)
     return st;
@@ -389,6 +393,7 @@ extern "C" cc_status cc_attn_scores_exp(const cc_bf16* q, const cc_bf16* k, cc_b
 extern "C" cc_status cc_attn_exp_rescale(cc_bf16* e, float* stats, int t, int hw, int64_t ld_e, void* stream) {
   const char* what = "attn_exp_rescale";
   cc_status st;
+  if (empty_request(what, {t, hw}, &st)) return st;
   if ((st = check_ptr(what, e)) != CC_OK || (st = check_ptr(what, stats)) != CC_OK) return st;
   if (t <= 0 || hw <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
   if (ld_e < hw || ld_e % 8) return fail(CC_ERR_INVALID, "%s: need ld_e >= HW and ld_e %% 8 == 0", what);
@@ -408,6 +413,7 @@ extern "C" cc_status cc_attn_pv_exp(const cc_bf16* e, const float* stats, const 
                                     int c, int64_t ld_e, int64_t ld_v, int64_t ld_o, void* stream) {
   const char* what = "attn_pv_exp";
   cc_status st;
+  if (empty_request(what, {t, hw}, &st)) return st;
   if ((st = check_ptr(what, e)) != CC_OK || (st = check_ptr(what, stats)) != CC_OK ||
       (st = check_ptr(what, v)) != CC_OK || (st = check_ptr(what, o)) != CC_OK)
     return st;
@@ -443,9 +449,9 @@ extern "C" cc_status cc_attn_frame_exp(const cc_bf16* q, const cc_bf16* k, const
                                        int c, int64_t ld_q, int64_t ld_k, int64_t ld_v, int64_t ld_o, float scale,
                                        void* ws, size_t ws_bytes, void* stream) {
   const char* what = "attn_frame_exp";
-  if (t <= 0 || hw <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
-  cc_status st = check_ptr(what, ws);
-  if (st != CC_OK) return st;
+  cc_status st;
+  if (empty_request(what, {t, hw}, &st)) return st;
+  if ((st = check_ptr(what, ws)) != CC_OK) return st;
   const size_t need = cc_attn_exp_workspace_bytes(t, hw);
   if (ws_bytes < need) return fail(CC_ERR_INVALID, "%s: workspace of %zu bytes, need %zu", what, ws_bytes, need);
   const int64_t ld = cc_attn_ld(hw);

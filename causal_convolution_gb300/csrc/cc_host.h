@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstddef>
 #include <cstdint>
+#include <initializer_list>
 #include <utility>
 
 #include "cc.h"
@@ -20,6 +21,12 @@ namespace cc {
 cc_status fail(cc_status st, const char* fmt, ...);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A request whose output covers no position (a zero batch, frame, row,
+// column or per-frame position count) has nothing to compute: it succeeds
+// before any other check, launching nothing and reading no pointer. A
+// negative count is invalid. Returns true when the caller is to return *st.
+bool empty_request(const char* what, std::initializer_list<long long> counts, cc_status* st);
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel on the stream is still finishing (its CTAs take

@@ -121,8 +121,9 @@ extern "C" cc_status cc_conv3d_prepare(const cc_bf16* w, cc_bf16* wp, int cout, 
 extern "C" cc_status cc_conv3d_causal(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* y, int n,
                                       int d, int h, int w, int cin, int cout, int hist, void* stream) {
   const char* what = "conv3d_causal";
-  cc_status st = check_ptrs(what, {x, wp, y});
-  if (st != CC_OK) return st;
+  cc_status st;
+  if (empty_request(what, {n, d, h, w}, &st)) return st;
+  if ((st = check_ptrs(what, {x, wp, y})) != CC_OK) return st;
   if (bias && !aligned16(bias)) return fail(CC_ERR_INVALID, "%s: bias must be 16-byte aligned", what);
   if ((st = check_grid(what, n, d, h, w, hist)) != CC_OK) return st;
   if (cin <= 0 || cout <= 0) return fail(CC_ERR_INVALID, "%s: channel counts must be positive", what);
@@ -199,8 +200,9 @@ extern "C" cc_status cc_resample_prepare_temporal(const cc_bf16* w, cc_bf16* pw,
 extern "C" cc_status cc_resample_phase_conv(const cc_bf16* x, const cc_bf16* pw, cc_bf16* phases, int n, int d,
                                             int hl, int wl, int cin, int cout, int hist, void* stream) {
   const char* what = "resample_phase_conv";
-  cc_status st = check_ptrs(what, {x, pw, phases});
-  if (st != CC_OK) return st;
+  cc_status st;
+  if (empty_request(what, {n, d, hl, wl}, &st)) return st;
+  if ((st = check_ptrs(what, {x, pw, phases})) != CC_OK) return st;
   if ((st = check_grid(what, n, d, hl, wl, hist)) != CC_OK) return st;
   if (cin <= 0 || cout <= 0) return fail(CC_ERR_INVALID, "%s: channel counts must be positive", what);
   if (cin % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C_in must be a multiple of 64 (got %d)", what, cin);
@@ -255,8 +257,9 @@ extern "C" cc_status cc_resample_up2_fused(const cc_bf16* x, const cc_bf16* pw, 
                                            const cc_bf16* skip, cc_bf16* out, int n, int d, int hl, int wl, int cin,
                                            int cout, int hist, int temporal, void* stream) {
   const char* what = "resample_up2_fused";
-  cc_status st = check_ptrs(what, {x, pw, bias, skip, out});
-  if (st != CC_OK) return st;
+  cc_status st;
+  if (empty_request(what, {n, d, hl, wl}, &st)) return st;
+  if ((st = check_ptrs(what, {x, pw, bias, skip, out})) != CC_OK) return st;
   if ((st = check_grid(what, n, d, hl, wl, hist)) != CC_OK) return st;
   if (temporal != 0 && temporal != 1) return fail(CC_ERR_INVALID, "%s: temporal must be 0 or 1", what);
   if (cin <= 0 || cout <= 0) return fail(CC_ERR_INVALID, "%s: channel counts must be positive", what);

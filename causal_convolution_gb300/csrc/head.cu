@@ -390,6 +390,7 @@ extern "C" cc_status cc_head_temporal(const cc_bf16* x, const cc_bf16* wp, cc_bf
                                       int cin, int hist, void* stream) {
   const char* what = "head_temporal";
   cc_status st;
+  if (empty_request(what, {n, d, h, w}, &st)) return st;
   if ((st = check_ptr(what, x)) != CC_OK || (st = check_ptr(what, wp)) != CC_OK || (st = check_ptr(what, g)) != CC_OK)
     return st;
   if (n <= 0 || d <= 0 || h <= 0 || w <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);

@@ -56,6 +56,19 @@ cc_status fail(cc_status st, const char* fmt, ...) {
   return st;
 }
 
+bool empty_request(const char* what, std::initializer_list<long long> counts, cc_status* st) {
+  bool empty = false;
+  for (long long c : counts) {
+    if (c < 0) {
+      *st = fail(CC_ERR_INVALID, "%s: sizes must not be negative", what);
+      return true;
+    }
+    empty = empty || c == 0;
+  }
+  *st = CC_OK;
+  return empty;
+}
+
 cc_status launch_status(const char* what) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));

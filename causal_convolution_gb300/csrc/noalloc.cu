@@ -62,7 +62,8 @@ using namespace cc;
 extern "C" cc_status cc_head_out_noalloc(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* out,
                                          int n, int d, int h, int w, int cin, int hist, void* stream) {
   const char* what = "head_out_noalloc";
-  if (n <= 0 || d <= 0 || h <= 0 || w <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
+  cc_status st;
+  if (empty_request(what, {n, d, h, w}, &st)) return st;
   const long long positions = (long long)n * d * h * w;
   const long long max_positions = (long long)(CC_HEAD_NOALLOC_SCRATCH_BYTES / (CC_HEAD_G_CH * 2));
   if (positions > max_positions)
@@ -72,8 +73,7 @@ extern "C" cc_status cc_head_out_noalloc(const cc_bf16* x, const cc_bf16* wp, co
                 what, positions, positions * CC_HEAD_G_CH * 2, (long long)CC_HEAD_NOALLOC_SCRATCH_BYTES,
                 max_positions);
   void* g = nullptr;
-  cc_status st = scratch_address(&g);
-  if (st != CC_OK) return st;
+  if ((st = scratch_address(&g)) != CC_OK) return st;
   if ((st = cc_head_temporal(x, wp, static_cast<cc_bf16*>(g), n, d, h, w, cin, hist, stream)) != CC_OK) return st;
   return cc_head_stencil(static_cast<const cc_bf16*>(g), bias, out, n, d, h, w, stream);
 }

@@ -220,6 +220,7 @@ extern "C" cc_status cc_resample_interleave(const cc_bf16* phases, const cc_bf16
                                             cc_bf16* out, int n, int d, int hl, int wl, int c, void* stream) {
   const char* what = "resample_interleave";
   cc_status st;
+  if (empty_request(what, {n, d, hl, wl}, &st)) return st;
   if ((st = check_ptr(what, phases)) != CC_OK || (st = check_ptr(what, bias)) != CC_OK ||
       (st = check_ptr(what, skip)) != CC_OK || (st = check_ptr(what, out)) != CC_OK)
     return st;
@@ -244,10 +245,11 @@ extern "C" cc_status cc_resample_up2(const cc_bf16* x, const cc_bf16* pw, const 
                                      cc_bf16* out, int n, int d, int hl, int wl, int cin, int cout, int hist,
                                      void* ws, size_t ws_bytes, void* stream) {
   const char* what = "resample_up2";
-  cc_status st = check_ptr(what, ws);
-  if (st != CC_OK) return st;
+  cc_status st;
+  if (empty_request(what, {n, d, hl, wl}, &st)) return st;
+  if ((st = check_ptr(what, ws)) != CC_OK) return st;
   const size_t need = cc_resample_workspace_bytes(n, d, hl, wl, cout);
-  if (need == 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
+  if (need == 0) return fail(CC_ERR_INVALID, "%s: channel counts must be positive", what);
   if (ws_bytes < need) return fail(CC_ERR_INVALID, "%s: workspace of %zu bytes, need %zu", what, ws_bytes, need);
   cc_bf16* phases = static_cast<cc_bf16*>(ws);
   if ((st = cc_resample_phase_conv(x, pw, phases, n, d, hl, wl, cin, cout, hist, stream)) != CC_OK) return st;
@@ -263,6 +265,7 @@ extern "C" cc_status cc_head_stencil(const cc_bf16* g, const cc_bf16* bias, cc_b
                                      void* stream) {
   const char* what = "head_stencil";
   cc_status st;
+  if (empty_request(what, {n, d, h, w}, &st)) return st;
   if ((st = check_ptr(what, g)) != CC_OK || (st = check_ptr(what, bias)) != CC_OK ||
       (st = check_ptr(what, out)) != CC_OK)
     return st;
@@ -298,10 +301,10 @@ extern "C" cc_status cc_head_stencil(const cc_bf16* g, const cc_bf16* bias, cc_b
 extern "C" cc_status cc_head_out(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* out, int n, int d,
                                  int h, int w, int cin, int hist, void* ws, size_t ws_bytes, void* stream) {
   const char* what = "head_out";
-  cc_status st = check_ptr(what, ws);
-  if (st != CC_OK) return st;
+  cc_status st;
+  if (empty_request(what, {n, d, h, w}, &st)) return st;
+  if ((st = check_ptr(what, ws)) != CC_OK) return st;
   const size_t need = cc_head_workspace_bytes(n, d, h, w);
-  if (need == 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
   if (ws_bytes < need) return fail(CC_ERR_INVALID, "%s: workspace of %zu bytes, need %zu", what, ws_bytes, need);
   cc_bf16* g = static_cast<cc_bf16*>(ws);
   if ((st = cc_head_temporal(x, wp, g, n, d, h, w, cin, hist, stream)) != CC_OK) return st;

@@ -24,6 +24,10 @@
  *    launches nothing and returns CC_ERR_INVALID or CC_ERR_UNSUPPORTED;
  *    cc_last_error() then describes the reason. No C++ exception crosses
  *    the ABI.
+ *  - A request whose output covers no position (a count of images, frames,
+ *    rows, columns or per-frame positions is 0) succeeds at once: it
+ *    launches nothing and reads none of its pointers, which may be NULL.
+ *    Negative counts are CC_ERR_INVALID; channel counts must be positive.
  *  - Kernels never trap. A pipeline wait that runs past its time limit makes
  *    the kernel wind down and set a device error word, which
  *    cc_check_device() reports as CC_ERR_TIMEOUT.

@@ -98,3 +98,34 @@ def test_host_validation_rejects_before_any_launch(lib):
     assert b"workspace" in lib.cc_last_error()
     assert lib.cc_debug_wait_timeout(0, None) == 1
     assert lib.cc_debug_im2col_tile(p, p, 1, 1, 1, 1, 64, -17, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == 1
+
+
+def test_empty_requests_succeed_without_a_launch(lib):
+    # a zero count of images, frames, rows, columns or positions: CC_OK with
+    # NULL pointers and no device (nothing is launched, no pointer is read)
+    f = ctypes.c_float(0.125)
+    assert lib.cc_conv3d_causal(None, None, None, None, 0, 4, 8, 8, 64, 64, 0, None) == 0
+    assert lib.cc_conv3d_causal(None, None, None, None, 1, 0, 8, 8, 64, 64, 2, None) == 0
+    assert lib.cc_conv3d_causal(None, None, None, None, 1, 4, 8, 0, 64, 64, 0, None) == 0
+    assert lib.cc_resample_phase_conv(None, None, None, 1, 1, 0, 4, 64, 64, 0, None) == 0
+    assert lib.cc_resample_interleave(None, None, None, None, 1, 0, 4, 4, 64, None) == 0
+    assert lib.cc_resample_up2(None, None, None, None, None, 0, 1, 4, 4, 64, 64, 0, None, 0, None) == 0
+    assert lib.cc_resample_up2_fused(None, None, None, None, None, 1, 1, 4, 0, 64, 64, 0, 1, None) == 0
+    assert lib.cc_attn_scores(None, None, None, 0, 16, 64, 64, 64, 16, None) == 0
+    assert lib.cc_attn_softmax(None, None, 2, 0, 16, 16, f, None) == 0
+    assert lib.cc_attn_pv(None, None, None, 0, 16, 64, 16, 64, 64, None) == 0
+    assert lib.cc_attn_frame(None, None, None, None, 2, 0, 64, 64, 64, 64, 64, f, None, 0, None) == 0
+    assert lib.cc_attn_scores_exp(None, None, None, None, 0, 16, 64, 64, 64, 16, f, None) == 0
+    assert lib.cc_attn_exp_rescale(None, None, 3, 0, 16, None) == 0
+    assert lib.cc_attn_pv_exp(None, None, None, None, 0, 16, 64, 16, 64, 64, None) == 0
+    assert lib.cc_attn_frame_exp(None, None, None, None, 0, 5, 64, 64, 64, 64, 64, f, None, 0, None) == 0
+    assert lib.cc_head_temporal(None, None, None, 1, 0, 4, 4, 256, 0, None) == 0
+    assert lib.cc_head_stencil(None, None, None, 1, 2, 0, 4, None) == 0
+    assert lib.cc_head_out(None, None, None, None, 0, 2, 4, 4, 256, 0, None, 0, None) == 0
+    assert lib.cc_head_out_noalloc(None, None, None, None, 1, 0, 4, 4, 256, 2, None) == 0
+    assert lib.cc_attn_exp_workspace_bytes(0, 16) == 0 and lib.cc_head_workspace_bytes(1, 0, 4, 4) == 0
+    # a negative count stays invalid, whatever the other counts
+    assert lib.cc_conv3d_causal(None, None, None, None, 0, -1, 8, 8, 64, 64, 0, None) == 1
+    assert b"negative" in lib.cc_last_error()
+    assert lib.cc_attn_frame_exp(None, None, None, None, -2, 0, 64, 64, 64, 64, 64, f, None, 0, None) == 1
+    assert lib.cc_head_out_noalloc(None, None, None, None, 1, 1, -4, 4, 256, 0, None) == 1

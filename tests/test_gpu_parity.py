@@ -419,6 +419,29 @@ def test_unsupported_and_invalid_requests_raise():
     api.cc_check_device()
 
 
+def test_empty_tensors_are_a_no_op():
+    # zero frames, rows or positions: every entry point returns at once
+    wp = empty(27 * 64 * 64)
+    api.cc_conv3d_causal(empty(1, 2, 4, 4, 64), wp, None, empty(1, 0, 4, 4, 64), hist=2)
+    api.cc_conv3d_causal(empty(0, 3, 4, 4, 64), wp, None, empty(0, 3, 4, 4, 64))
+    pw = empty(48 * 64 * 64)
+    b, skip = empty(64), empty(1, 3, 0, 4, 64)
+    api.cc_resample_up2_fused(empty(1, 3, 0, 4, 64), pw, b, skip, empty(1, 3, 0, 8, 64))
+    api.cc_resample_up2(empty(1, 3, 0, 4, 64), pw, b, skip, empty(1, 3, 0, 8, 64),
+                        torch.empty(0, dtype=torch.uint8, device=DEV))
+    q = empty(2, 0, 64)
+    api.cc_attn_frame_exp(q, q, q, empty(2, 0, 64), torch.empty(0, dtype=torch.uint8, device=DEV))
+    api.cc_attn_frame(q, q, q, empty(2, 0, 64), torch.empty(0, dtype=torch.uint8, device=DEV))
+    hw = empty(3 * api.HEAD_G_CH * 64)
+    api.cc_head_out(empty(1, 0, 4, 4, 64), hw, empty(12), empty(1, 0, 4, 4, 12),
+                    torch.empty(0, dtype=torch.uint8, device=DEV))
+    api.cc_head_out_noalloc(empty(1, 2, 4, 0, 64), hw, empty(12), empty(1, 0, 4, 0, 12), hist=2)
+    api.cc_check_device()
+    # the library is still usable afterwards
+    inp, _, y = run_conv(1, 2, 3, 5, 64, 16, 0)
+    assert_parity(to_np(y), oracle.causal_conv3d(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"])), "conv after")
+
+
 def test_kernel_wait_timeout_is_reported_and_cleared():
     api.cc_debug_wait_timeout(2_000_000)
     with pytest.raises(api.CCError) as e:
