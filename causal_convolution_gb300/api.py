@@ -180,7 +180,7 @@ def cc_attn_workspace_bytes(t: int, hw: int) -> int:
 
 def _rows(t: torch.Tensor, name: str):
     """(T, HW, C, ld) of a [T, HW, C] tensor whose rows may be strided (packed qkv slices)."""
-    if t.dim() != 3 or t.stride(2) != 1 or t.stride(0) != t.shape[1] * t.stride(1):
+    if t.dim() != 3 or (t.numel() and (t.stride(2) != 1 or t.stride(0) != t.shape[1] * t.stride(1))):
         raise ValueError(f"{name}: expected [T,HW,C] with unit channel stride and frame stride HW*ld")
     if t.device.type != "cuda" or t.dtype != torch.bfloat16:
         raise ValueError(f"{name}: expected a bf16 CUDA tensor")
