@@ -115,14 +115,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Pull a tile into L2 ahead of its shared-memory load (no completion signal).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 // im2col load over a rank-5 [N, D, H, W, C] tensor: `pixelsPerColumn` output
 // pixels starting at (w, h, d, n) inside the map's bounding box, each pixel
 // read at (w + ow, h + oh, d + od), channels c .. c + channelsPerPixel - 1;
