@@ -58,10 +58,12 @@ __device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, in
 template <int AMODE>
 __device__ __forceinline__ int tile_first_tap(const GemmArgs& a, int batch, int mp) {
   if (AMODE != kAIm2col || a.lo_d >= 0) return 0;
-  const long long plane = static_cast<long long>(a.img_h) * a.img_w;
-  const long long per_image = plane * a.img_d;
-  const long long m0 = static_cast<long long>(mp) * 2 * kBlockM;
-  const long long m1 = min(m0 + 2 * kBlockM, static_cast<long long>(a.m_total)) - 1;
+  // 32-bit arithmetic (m_total < 2^31 - 1024): the MMA thread runs this
+  // between two tiles, where 64-bit divisions showed up as idle tensor cycles
+  const unsigned plane = static_cast<unsigned>(a.img_h) * a.img_w;
+  const unsigned per_image = plane * a.img_d;
+  const unsigned m0 = static_cast<unsigned>(mp) * 2 * kBlockM;
+  const unsigned m1 = min(m0 + 2 * kBlockM, static_cast<unsigned>(a.m_total)) - 1;
   // the latest frame any row of the tile lies in (a tile across an image
   // boundary holds the previous image's last frame)
   const int t_max = m0 / per_image != m1 / per_image ? a.img_d - 1 : static_cast<int>((m1 / plane) % a.img_d);
