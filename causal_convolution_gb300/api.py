@@ -23,7 +23,7 @@ __all__ = [
     "cc_attn_exp_key_tiles", "cc_attn_exp_workspace_bytes", "cc_attn_scores_exp", "cc_attn_exp_rescale",
     "cc_attn_pv_exp", "cc_attn_frame_exp",
     "cc_head_prepare", "cc_head_workspace_bytes", "cc_head_temporal", "cc_head_stencil", "cc_head_out",
-    "cc_head_out_noalloc", "HEAD_NOALLOC_SCRATCH_BYTES",
+    "cc_head_out_noalloc", "HEAD_NOALLOC_SCRATCH_BYTES", "cc_copy_to_host",
     "cc_debug_im2col_tile", "cc_debug_wait_timeout",
     "HEAD_COUT", "HEAD_G_CH",
 ]
@@ -333,6 +333,25 @@ def cc_head_out_noalloc(x, wp, bias, out, hist: int = 0, stream=None) -> None:
         raise ValueError("head_out_noalloc: out must be [N,D,H,W,12] of x [N,D+hist,H,W,Cin]")
     _check(_lib.load().cc_head_out_noalloc(_ptr(x, name="x"), _ptr(wp, name="wp"), _ptr(bias, name="bias"),
                                            _ptr(out, name="out"), n, d, h, w, cin, hist, _stream(stream)))
+
+
+# -------------------------------------------------------- result read-back --
+
+def cc_copy_to_host(dst: torch.Tensor, src: torch.Tensor, ctas: int = 8, stream=None) -> None:
+    """Copies the CUDA tensor `src` into the pinned CPU tensor `dst` (same
+    number of bytes, both contiguous) with a copy kernel of `ctas` CTAs."""
+    if not isinstance(dst, torch.Tensor) or not isinstance(src, torch.Tensor):
+        raise TypeError("copy_to_host: expected torch tensors")
+    if dst.device.type != "cpu" or not dst.is_pinned():
+        raise ValueError("copy_to_host: dst must be a pinned CPU tensor")
+    if src.device.type != "cuda":
+        raise ValueError("copy_to_host: src must be a CUDA tensor")
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy_to_host: tensors must be contiguous")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("copy_to_host: dst and src hold different numbers of bytes")
+    _check(_lib.load().cc_copy_to_host(dst.data_ptr(), src.data_ptr(), nbytes, int(ctas), _stream(stream)))
 
 
 # ------------------------------------------------------------- self tests --

@@ -48,6 +48,7 @@
  *         a 3x3 stencil, bias and clamp) and head_stencil_kernel.
  *  [STACK] the stack's definition: causal 3x3x3 conv with two history frames,
  *         zeros before frame 0, spatial zero padding 1, fp32 accumulation.
+ *  [HOST] no page: a transfer helper for the chunk-by-chunk decode loop.
  */
 #ifndef CC_H_
 #define CC_H_
@@ -284,6 +285,26 @@ cc_status cc_head_out(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, 
  * Other arguments, layouts and errors as cc_head_out. */
 cc_status cc_head_out_noalloc(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* out, int n, int d,
                               int h, int w, int cin, int hist, void* stream);
+
+/* ------------------------------------------------- result read-back [HOST] */
+
+/* Copies `bytes` from device memory at `src` to page-locked host memory at
+ * `dst` with a copy kernel of `ctas` thread blocks on `stream`, for a chunked
+ * decode whose outputs go back to the host while the next chunk's inputs
+ * come in. Not part of the method: a transfer helper. A copy-engine read-back
+ * (cudaMemcpyAsync) beside a host-to-device copy takes about half of the host
+ * link from it; the SMs' stores to the mapped host address run at a rate set
+ * by `ctas` (4-8: ~90 GB/s measured on GB300) and leave the inflowing copy
+ * nearly its whole bandwidth.
+ *  - dst: page-locked host memory (cudaHostAlloc, cudaHostRegister) that the
+ *    device addresses at the same pointer (unified addressing); src: device
+ *    memory; both 16-byte aligned, `bytes` a multiple of 16, 1 <= ctas <= 1024.
+ *    Both ends of each range are checked with cudaPointerGetAttributes;
+ *    anything else is CC_ERR_INVALID and nothing is launched. bytes == 0
+ *    succeeds at once.
+ *  - Asynchronous on `stream`; `dst` holds the data once the stream's work up
+ *    to this call is done. The caller keeps both buffers alive until then. */
+cc_status cc_copy_to_host(void* dst, const void* src, size_t bytes, int ctas, void* stream);
 
 #ifdef __cplusplus
 }

@@ -129,3 +129,19 @@ def test_empty_requests_succeed_without_a_launch(lib):
     assert b"negative" in lib.cc_last_error()
     assert lib.cc_attn_frame_exp(None, None, None, None, -2, 0, 64, 64, 64, 64, 64, f, None, 0, None) == 1
     assert lib.cc_head_out_noalloc(None, None, None, None, 1, 1, -4, 4, 256, 0, None) == 1
+
+
+def test_copy_to_host_argument_checks(lib):
+    buf = ctypes.create_string_buffer(1 << 12)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.cc_copy_to_host(None, None, 0, 8, None) == 0  # nothing to copy
+    assert lib.cc_copy_to_host(None, p, 64, 8, None) == 1
+    assert lib.cc_copy_to_host(p + 4, p, 64, 8, None) == 1
+    assert b"aligned" in lib.cc_last_error()
+    assert lib.cc_copy_to_host(p, p, 40, 8, None) == 1
+    assert b"multiple of 16" in lib.cc_last_error()
+    assert lib.cc_copy_to_host(p, p, 64, 0, None) == 1 and lib.cc_copy_to_host(p, p, 64, 1025, None) == 1
+    # memory the device cannot address (no device here at all): rejected, not launched
+    assert lib.cc_copy_to_host(p, p, 64, 8, None) == 1
+    assert b"page-locked" in lib.cc_last_error()
+

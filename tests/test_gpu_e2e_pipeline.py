@@ -55,3 +55,41 @@ def test_pipelined_chunks_match_resident_step():
     for c in range(chunks):
         for n, ref in refs[c % 2].items():
             assert torch.equal(outs[c][n], ref), f"chunk {c}: {n} differs from the resident step"
+
+
+@pytest.mark.parametrize("nbytes,ctas", [(16, 1), (4096 + 16, 3), ((1 << 20) + 48, 8), (100 << 20, 8), (64 << 20, 152)])
+def test_copy_to_host_is_a_byte_copy(nbytes, ctas):
+    from causal_convolution_gb300 import api
+
+    g = torch.Generator(device="cuda").manual_seed(nbytes)
+    src = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda", generator=g)
+    dst = torch.zeros(nbytes, dtype=torch.uint8, pin_memory=True)
+    stream = torch.cuda.Stream()
+    api.cc_copy_to_host(dst, src, ctas=ctas, stream=stream)
+    stream.synchronize()
+    api.cc_check_device()
+    assert torch.equal(dst, src.cpu())
+
+
+def test_copy_to_host_rejects_what_the_device_cannot_address():
+    from causal_convolution_gb300 import _lib, api
+
+    lib = _lib.load()
+    n = 1 << 16
+    src = torch.ones(n, dtype=torch.uint8, device="cuda")
+    pinned = torch.zeros(n, dtype=torch.uint8, pin_memory=True)
+    pageable = torch.zeros(n, dtype=torch.uint8)
+    dev_dst = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    # pageable host memory, device memory as the destination, pinned memory as
+    # the source, a ragged size: rejected on the host, nothing launched
+    assert lib.cc_copy_to_host(pageable.data_ptr(), src.data_ptr(), n, 8, None) == 1
+    assert b"page-locked" in lib.cc_last_error()
+    assert lib.cc_copy_to_host(dev_dst.data_ptr(), src.data_ptr(), n, 8, None) == 1
+    assert lib.cc_copy_to_host(pinned.data_ptr(), pinned.data_ptr(), n, 8, None) == 1
+    assert b"device memory" in lib.cc_last_error()
+    assert lib.cc_copy_to_host(pinned.data_ptr(), src.data_ptr(), n - 8, 8, None) == 1
+    with pytest.raises(ValueError):
+        api.cc_copy_to_host(pageable, src)
+    torch.cuda.synchronize()
+    api.cc_check_device()
+    assert int(pinned.sum()) == 0
