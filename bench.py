@@ -333,39 +333,31 @@ class Workload:
               ("res", ("res_x", "res_skip"), ("res_out",)),
               ("head", ("head_x",), ("head_out",)))
 
-    def host_buffers(self, copy_streams: int = 1):
+    def host_buffers(self):
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
         self.d_in = {"conv_x": self.conv_x, "q": self.q, "k": self.k, "v": self.v, "res_x": self.res_x,
                      "res_skip": self.res_skip, "head_x": self.head_x}
         self.d_out = {"conv_y": self.conv_y, "o": self.o, "res_out": self.res_out, "head_out": self.head_out}
         self.h_in = {n: pin(t) for n, t in self.d_in.items()}
         self.h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in self.d_out.items()}
-        dev = self.dev
-        self.s_h2d = [torch.cuda.Stream(dev) for _ in range(copy_streams)]
-        self.s_d2h = [torch.cuda.Stream(dev) for _ in range(copy_streams)]
-        ev = lambda: torch.cuda.Event()
+        # one copy-in stream (more streams gave no more host-link bandwidth) and
+        # one read-back stream
+        self.s_h2d = torch.cuda.Stream(self.dev)
+        self.s_d2h = torch.cuda.Stream(self.dev)
         nst = len(self.STAGES)
-        self.ev_in = [[ev() for _ in self.s_h2d] for _ in range(nst)]     # stage inputs landed
-        self.ev_used = [ev() for _ in range(nst)]                          # stage kernels done
-        self.ev_out = [[ev() for _ in self.s_d2h] for _ in range(nst)]    # stage outputs read back
+        self.ev_in = [torch.cuda.Event() for _ in range(nst)]    # stage inputs landed
+        self.ev_used = [torch.cuda.Event() for _ in range(nst)]  # stage kernels done
+        self.ev_out = [torch.cuda.Event() for _ in range(nst)]   # stage outputs read back
         self.e2e_primed = False
         h2d = sum(t.numel() * t.element_size() for t in self.h_in.values())
         d2h = sum(t.numel() * t.element_size() for t in self.h_out.values())
         return h2d, d2h
 
-    @staticmethod
-    def _split(dst, src, k):
-        """k contiguous, element-aligned slices of a copy dst <- src."""
-        a, b = dst.view(-1), src.view(-1)
-        n = a.numel()
-        step = -(-n // k)
-        return [(a[i:i + step], b[i:i + step]) for i in range(0, n, step)]
-
     def step_e2e(self, stream, h_in=None, h_out=None):
         """One chunk from pinned host inputs (`h_in`, default the ones
         `host_buffers` made) to pinned host outputs (`h_out`): the same
         seven launches as `step`. Inputs go in stage by stage on the copy-in
-        streams, each stage's launches wait only for their own inputs, and each
+        stream, each stage's launches wait only for their own inputs, and each
         output goes back as soon as its stage ends, so copies overlap compute
         (and the previous chunk's copies) but never a buffer still in use:
         a stage's inputs are rewritten only after its kernels of the previous
@@ -375,33 +367,26 @@ class Workload:
         launches = self.launches(stream)
         for i, (_, ins, _) in enumerate(self.STAGES):
             if self.e2e_primed:
-                for s in self.s_h2d:
-                    s.wait_event(self.ev_used[i])
-            for name in ins:
-                for j, (d, h) in enumerate(self._split(self.d_in[name], h_in[name], len(self.s_h2d))):
-                    with torch.cuda.stream(self.s_h2d[j]):
-                        d.copy_(h, non_blocking=True)
-            for j, s in enumerate(self.s_h2d):
-                self.ev_in[i][j].record(s)
+                self.s_h2d.wait_event(self.ev_used[i])
+            with torch.cuda.stream(self.s_h2d):
+                for name in ins:
+                    self.d_in[name].copy_(h_in[name], non_blocking=True)
+            self.ev_in[i].record(self.s_h2d)
         for i, (stage, _, outs) in enumerate(self.STAGES):
-            for j in range(len(self.s_h2d)):
-                stream.wait_event(self.ev_in[i][j])
+            stream.wait_event(self.ev_in[i])
             if self.e2e_primed:
-                for j in range(len(self.s_d2h)):
-                    stream.wait_event(self.ev_out[i][j])
+                stream.wait_event(self.ev_out[i])
             for st, launch in launches:
                 if st == stage:
                     launch()
             self.ev_used[i].record(stream)
-            for j, s in enumerate(self.s_d2h):
-                s.wait_event(self.ev_used[i])
+            self.s_d2h.wait_event(self.ev_used[i])
             # read back by the library's copy kernel (a few CTAs storing to
             # the mapped pinned buffers): beside the copy-engine copy-in it
             # leaves that copy nearly its whole link bandwidth
             for name in outs:
-                self.api.cc_copy_to_host(h_out[name], self.d_out[name], ctas=E2E_READBACK_CTAS, stream=self.s_d2h[0])
-            for j, s in enumerate(self.s_d2h):
-                self.ev_out[i][j].record(s)
+                self.api.cc_copy_to_host(h_out[name], self.d_out[name], ctas=E2E_READBACK_CTAS, stream=self.s_d2h)
+            self.ev_out[i].record(self.s_d2h)
         self.e2e_primed = True
 
 
