@@ -124,6 +124,14 @@ __global__ void __launch_bounds__(kSoftmaxWarps * 32) softmax_rows_long_kernel(c
   for (long long c = hw + lane; c < ld_p; c += 32) pr[c] = __float2bfloat16_rn(0.f);
 }
 
+// Per-frame GEMMs: 128-row tiles of the HW queries times 256-column tiles of
+// the keys (or channels), for every frame, must be countable in an int.
+cc_status check_tiles(const char* what, int t, int rows, int cols) {
+  if ((long long)((rows + 127) / 128) * ((cols + 255) / 256) * t > 0x7fffffffLL)
+    return fail(CC_ERR_UNSUPPORTED, "%s: too many output tiles", what);
+  return CC_OK;
+}
+
 cc_status check_ptr(const char* what, const void* p) {
   if (!p) return fail(CC_ERR_INVALID, "%s: null pointer", what);
   if (!aligned16(p)) return fail(CC_ERR_INVALID, "%s: pointers must be 16-byte aligned", what);
@@ -154,6 +162,7 @@ extern "C" cc_status cc_attn_scores(const cc_bf16* q, const cc_bf16* k, float* s
     return st;
   if (t <= 0 || hw <= 0 || c <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
   if (c % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C must be a multiple of 64 (got %d)", what, c);
+  if ((st = check_tiles(what, t, hw, hw)) != CC_OK) return st;
   if (ld_q < c || ld_k < c || ld_s < hw) return fail(CC_ERR_INVALID, "%s: row strides too small", what);
   if (ld_q % 8 || ld_k % 8 || ld_s % 4)
     return fail(CC_ERR_INVALID, "%s: ld_q, ld_k must be multiples of 8 and ld_s of 4", what);
@@ -228,6 +237,7 @@ extern "C" cc_status cc_attn_pv(const cc_bf16* p, const cc_bf16* v, cc_bf16* o, 
     return st;
   if (t <= 0 || hw <= 0 || c <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
   if (c % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C must be a multiple of 64 (got %d)", what, c);
+  if ((st = check_tiles(what, t, hw, c)) != CC_OK) return st;
   if (ld_p < hw || ld_v < c || ld_o < c) return fail(CC_ERR_INVALID, "%s: row strides too small", what);
   if (ld_p % 8 || ld_v % 8 || ld_o % 8) return fail(CC_ERR_INVALID, "%s: row strides must be multiples of 8", what);
   DeviceInfo di;
@@ -361,6 +371,7 @@ extern "C" cc_status cc_attn_scores_exp(const cc_bf16* q, const cc_bf16* k, cc_b
     return st;
   if (t <= 0 || hw <= 0 || c <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
   if (c % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C must be a multiple of 64 (got %d)", what, c);
+  if ((st = check_tiles(what, t, hw, hw)) != CC_OK) return st;
   if (ld_q < c || ld_k < c || ld_e < hw) return fail(CC_ERR_INVALID, "%s: row strides too small", what);
   if (ld_q % 8 || ld_k % 8 || ld_e % 8) return fail(CC_ERR_INVALID, "%s: row strides must be multiples of 8", what);
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CC_ERR_INVALID, "%s: scale must be finite and > 0", what);
@@ -419,6 +430,7 @@ extern "C" cc_status cc_attn_pv_exp(const cc_bf16* e, const float* stats, const 
     return st;
   if (t <= 0 || hw <= 0 || c <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
   if (c % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C must be a multiple of 64 (got %d)", what, c);
+  if ((st = check_tiles(what, t, hw, c)) != CC_OK) return st;
   if (ld_e < hw || ld_v < c || ld_o < c) return fail(CC_ERR_INVALID, "%s: row strides too small", what);
   if (ld_e % 8 || ld_v % 8 || ld_o % 8) return fail(CC_ERR_INVALID, "%s: row strides must be multiples of 8", what);
   DeviceInfo di;

@@ -13,6 +13,8 @@ template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = k
 cc_status launch_tc_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs& args, const DeviceInfo& di,
                          cudaStream_t stream, const char* what) {
   using S = GemmShape<BN>;
+  if ((long long)args.m_tiles * args.n_tiles * args.batches > 0x7fffffffLL)
+    return fail(CC_ERR_UNSUPPORTED, "%s: too many output tiles", what);
   if (args.num_tiles <= 0) return CC_OK;
   auto kern = tc_gemm_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
@@ -33,7 +35,9 @@ cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, Gemm
   using S = PairShape<BN, pair_staging_bytes<EPI>()>;
   if ((EPI == kEpiStoreF32 || EPI == kEpiExpBf16) && !tc)
     return fail(CC_ERR_INVALID, "%s: output tensor map missing", what);
-  args.num_tiles = ((args.m_tiles + 1) / 2) * args.n_tiles * args.batches;
+  const long long tiles = ((args.m_tiles + 1LL) / 2) * args.n_tiles * args.batches;
+  if (tiles > 0x7fffffffLL) return fail(CC_ERR_UNSUPPORTED, "%s: too many output tiles", what);
+  args.num_tiles = static_cast<int>(tiles);
   if (args.num_tiles <= 0) return CC_OK;
   auto kern = tc_gemm_pair_kernel<BN, AMODE, B_MN, OUT_F32, HAS_BIAS, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);

@@ -145,3 +145,22 @@ def test_copy_to_host_argument_checks(lib):
     assert lib.cc_copy_to_host(p, p, 64, 8, None) == 1
     assert b"page-locked" in lib.cc_last_error()
 
+
+
+def test_size_limits_rejected_on_the_host(lib):
+    # requests past the kernels' index ranges come back CC_ERR_UNSUPPORTED
+    # before any device call (no device here)
+    buf = ctypes.create_string_buffer(1 << 12)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16
+    big = 1 << 16
+    assert lib.cc_conv3d_causal(p, p, None, p, 1, 1, big, big, 64, 64, 0, None) == 2
+    assert b"too many positions" in lib.cc_last_error()
+    assert lib.cc_resample_up2_fused(p, p, p, p, p, 1, 1, big, big // 2, 64, 64, 0, 0, None) == 2
+    assert lib.cc_head_temporal(p, p, p, 1, 1, big, big, 256, 0, None) == 2
+    assert lib.cc_resample_interleave(p, p, p, p, 1, big, big, 1, 64, None) == 2
+    assert lib.cc_head_stencil(p, p, p, 1, big, big, big, None) == 2
+    hw = 1 << 30  # 2^23 query tiles x 2^22 key tiles
+    f = ctypes.c_float(0.125)
+    assert lib.cc_attn_scores_exp(p, p, p, p, 1, hw, 64, 64, 64, hw, f, None) == 2
+    assert b"too many output tiles" in lib.cc_last_error()
+    assert lib.cc_attn_scores(p, p, p, 1, hw, 64, 64, 64, hw, None) == 2
