@@ -453,8 +453,11 @@ extern "C" cc_status cc_attn_pv_exp(const cc_bf16* e, const float* stats, const 
   a.stats = const_cast<float2*>(reinterpret_cast<const float2*>(stats));
   a.stat_tiles = cc_attn_exp_key_tiles(hw);
   a.batch_outer = 1;  // frame by frame: one frame's v (7 MB at C=1024) serves every concurrent tile
-  return launch_tc_gemm_pair<256, kATiled3d, true, false, false, kEpiRowScale>(ta, tb, a, di,
-                                                                              static_cast<cudaStream_t>(stream), what);
+  // O leaves through TMA tensor stores of 64-channel x 128-row bf16 boxes
+  CUtensorMap tc;
+  if ((st = encode_tiled_3d(&tc, o, c, hw, t, 2ull * ld_o, 2ull * ld_o * hw, kBlockK, kBlockM)) != CC_OK) return st;
+  return launch_tc_gemm_pair<256, kATiled3d, true, false, false, kEpiRowScale>(
+      ta, tb, a, di, static_cast<cudaStream_t>(stream), what, &tc);
 }
 
 extern "C" cc_status cc_attn_frame_exp(const cc_bf16* q, const cc_bf16* k, const cc_bf16* v, cc_bf16* o, int t, int hw,

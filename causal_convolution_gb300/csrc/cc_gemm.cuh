@@ -64,7 +64,8 @@ struct GemmArgs {
   const __nv_bfloat16* skip;  // resampler epilogue: shortcut rows (row m at m * out_ld)
   int epi_tscale;             // resampler epilogue: 2 when the output is also x2 in time
   // softmax numerators in key tiles (kEpiExpBf16 writes them, kEpiRowScale
-  // reads them): per (batch, row, key tile) the pair (c_t, l_t)
+  // reads them to divide each output row by its sum): per (batch, row, key
+  // tile) the pair (c_t, l_t)
   float2* stats;
   int stat_tiles;   // key tiles per row
   float exp_k;      // scale * log2(e): exp(scale * s) = exp2(exp_k * s)
@@ -178,7 +179,7 @@ __device__ __forceinline__ void add_bf16x16(float (&v)[16], const __nv_bfloat16*
 // (skip row at soff): + bias, + shortcut, one rounding (or fp32 as is).
 template <bool OUT_F32, bool HAS_BIAS, int EPI>
 __device__ __forceinline__ void epi_store16(const GemmArgs& a, long long roff, long long soff, int n,
-                                            const uint32_t (&r)[16], float rscale = 1.f) {
+                                            const uint32_t (&r)[16]) {
   const bool full_chunk = n + 16 <= a.n_total;
   if constexpr (OUT_F32) {
     float* o = static_cast<float*>(a.out) + roff + n;
@@ -195,7 +196,7 @@ __device__ __forceinline__ void epi_store16(const GemmArgs& a, long long roff, l
   } else {
   float v[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) * (EPI == kEpiRowScale ? rscale : 1.f);
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + roff + n;
   if (full_chunk) {
     if (HAS_BIAS) add_bf16x16(v, a.bias + n);

@@ -33,7 +33,7 @@ template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = k
 cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs& args, const DeviceInfo& di,
                               cudaStream_t stream, const char* what, const CUtensorMap* tc = nullptr) {
   using S = PairShape<BN, pair_staging_bytes<EPI>()>;
-  if ((EPI == kEpiStoreF32 || EPI == kEpiExpBf16) && !tc)
+  if (pair_staging_bytes<EPI>() > 0 && !tc)
     return fail(CC_ERR_INVALID, "%s: output tensor map missing", what);
   const long long tiles = ((args.m_tiles + 1LL) / 2) * args.n_tiles * args.batches;
   if (tiles > 0x7fffffffLL) return fail(CC_ERR_UNSUPPORTED, "%s: too many output tiles", what);

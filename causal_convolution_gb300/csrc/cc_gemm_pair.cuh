@@ -88,7 +88,7 @@ constexpr int kStoreBufBytes = kBlockM * kStoreChunk * 4;  // 16 KB: 128 rows x 
 
 template <int EPI>
 constexpr int pair_staging_bytes() {
-  return (EPI == kEpiStoreF32 || EPI == kEpiExpBf16) ? 2 * kStoreBufBytes : 0;
+  return (EPI == kEpiStoreF32 || EPI == kEpiExpBf16 || EPI == kEpiRowScale) ? 2 * kStoreBufBytes : 0;
 }
 
 template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = kEpiPlain>
@@ -130,7 +130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
-    if (EPI == kEpiStoreF32 || EPI == kEpiExpBf16) tma_prefetch_map(&tmC);
+    if (pair_staging_bytes<EPI>() > 0) tma_prefetch_map(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), S::kTmemCols);
@@ -364,6 +364,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       }
     }
     if (issuer) bulk_wait_all();
+  } else if constexpr (EPI == kEpiRowScale) {
+    // -------- epilogue: row-scaled bf16 through staged TMA stores (both CTAs) --
+    // Each row's BN columns times 1 / l_row, packed to bf16 in 64-column
+    // chunks through the two swizzled staging buffers and one TMA tensor
+    // store per chunk (clipped at the last row), as in the numerators'
+    // epilogue: whole 128-byte row pieces leave the SM instead of 32-byte
+    // pieces of 128 rows, which held up the operand loads.
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const bool issuer = (warp == 2 && lane == 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int chunk = 0;
+    for (int k = 0, tile; (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
+      if (tile < 0) continue;
+      int batch, mp, nt;
+      pair_decode_tile(args, tile, batch, mp, nt);
+      if (!named_barrier_and(1, 128, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
+      tc_fence_after();
+      const int m0 = (2 * mp + static_cast<int>(rank)) * kBlockM;
+      const int n0 = nt * BN;
+      const int m = m0 + row;
+      float rscale = 0.f;  // rows past the end are staged but clipped by the store
+      if (m < args.m_total) {
+        float c_row, l_row;
+        row_stats(args, batch, m, c_row, l_row);
+        rscale = 1.f / l_row;
+      }
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * S::kAccCols;
+      const int valid = args.n_total - n0;
+      const int c64_end = valid >= BN ? BN / 64 : (valid + 63) / 64;
+#pragma unroll 1
+      for (int c = 0; c < c64_end; ++c, ++chunk) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32_wait(tbase + c * 64, r0);
+        tmem_ld32_wait(tbase + c * 64 + 32, r1);
+        if (c == c64_end - 1) {  // accumulator fully read: release it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t s0 = j < 16 ? r0[2 * j] : r1[2 * j - 32];
+          const uint32_t s1 = j < 16 ? r0[2 * j + 1] : r1[2 * j - 31];
+          __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(s0) * rscale, __uint_as_float(s1) * rscale);
+          pk[j] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        uint8_t* buf = sStage + (chunk & 1) * kStoreBufBytes;
+        if (issuer) bulk_wait_read_1();  // the store two chunks back has read this buffer
+        named_barrier_sync(1, 128);
+        uint8_t* rowp = buf + row * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(rowp + ((j ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (issuer) {
+          tma_store_3d(&tmC, smem_u32(buf), n0 + c * 64, m0, batch);
+          bulk_commit();
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (issuer) bulk_wait_all();
   } else if constexpr (EPI == kEpiStoreF32) {
     // ------------------------------ epilogue: staged TMA stores (both CTAs) --
     // Each 32-column chunk of the 128 x BN fp32 tile goes to one of two
@@ -436,14 +506,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * S::kAccCols;
       const long long roff = row_ok ? epi_row_offset<EPI>(args, batch, m) : 0;
       const long long soff = static_cast<long long>(m) * args.out_ld;
-      float rscale = 1.f;
-      if constexpr (EPI == kEpiRowScale) {
-        if (row_ok) {
-          float c_row, l_row;
-          row_stats(args, batch, m, c_row, l_row);
-          rscale = 1.f / l_row;
-        }
-      }
 #pragma unroll 1
       for (int c = 0; c < BN; c += 16) {
         uint32_t r[16];
@@ -451,7 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tmem_ld16(tbase + c, r);
         tmem_wait16(r);
         const int n = n0 + c;
-        if (row_ok && n < args.n_total) epi_store16<OUT_F32, HAS_BIAS, EPI>(args, roff, soff, n, r, rscale);
+        if (row_ok && n < args.n_total) epi_store16<OUT_F32, HAS_BIAS, EPI>(args, roff, soff, n, r);
       }
       tc_fence_before();
       __syncwarp();
