@@ -72,6 +72,9 @@ extern "C" cc_status cc_copy_to_host(void* dst, const void* src, size_t bytes, i
     return fail(CC_ERR_INVALID, "%s: dst must be page-locked host memory the device can address", what);
   if (!addressable_as(src, bytes, cudaMemoryTypeDevice))
     return fail(CC_ERR_INVALID, "%s: src must be device memory", what);
+  DeviceInfo di;  // the same device check as every other entry point
+  cc_status st = device_info(&di);
+  if (st != CC_OK) return st;
   copy_to_host_kernel<<<ctas, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(src), static_cast<uint4*>(dst), bytes / 16);
   return launch_status(what);
