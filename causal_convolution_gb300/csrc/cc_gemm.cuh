@@ -63,6 +63,10 @@ struct GemmArgs {
   const __nv_bfloat16* bias;  // per column, or nullptr
   const __nv_bfloat16* skip;  // resampler epilogue: shortcut rows (row m at m * out_ld)
   int epi_tscale;             // resampler epilogue: 2 when the output is also x2 in time
+  // 1 when every bf16 output row piece (and shortcut row piece) of 16
+  // columns starts on a 32-byte boundary: the epilogue then moves it with one
+  // 32-byte access instead of two 16-byte ones (set by the launcher)
+  int vec32;
   // softmax numerators in key tiles (kEpiExpBf16 writes them, kEpiRowScale
   // reads them to divide each output row by its sum): per (batch, row, key
   // tile) the pair (c_t, l_t)
@@ -200,13 +204,32 @@ __device__ __forceinline__ void epi_store16(const GemmArgs& a, long long roff, l
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + roff + n;
   if (full_chunk) {
     if (HAS_BIAS) add_bf16x16(v, a.bias + n);
-    if (EPI == kEpiResample) add_bf16x16(v, a.skip + soff + n);
+    if (EPI == kEpiResample) {
+      if (a.vec32) {
+        uint32_t s8[8];
+        ld_global_nc_v8(a.skip + soff + n, s8);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&s8[j]));
+          v[2 * j] += f.x;
+          v[2 * j + 1] += f.y;
+        }
+      } else {
+        add_bf16x16(v, a.skip + soff + n);
+      }
+    }
     uint4 pk[2];
     __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
     for (int j = 0; j < 8; ++j) p2[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-    reinterpret_cast<uint4*>(o)[0] = pk[0];
-    reinterpret_cast<uint4*>(o)[1] = pk[1];
+    // one 32-byte store per row piece where aligned: half as many, whole-sector
+    // L2 writes from a warp whose 32 lanes write 32 different rows
+    if (a.vec32) {
+      st_global_v8(o, pk);
+    } else {
+      reinterpret_cast<uint4*>(o)[0] = pk[0];
+      reinterpret_cast<uint4*>(o)[1] = pk[1];
+    }
   } else {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {

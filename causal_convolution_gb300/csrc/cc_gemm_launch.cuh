@@ -9,6 +9,13 @@
 
 namespace cc {
 
+// Whether the direct-store epilogue may use 32-byte accesses: every bf16 row
+// piece of 16 columns (output and shortcut) then starts on a 32-byte boundary.
+inline int epi_vec32(const GemmArgs& a, bool out_f32) {
+  const uintptr_t bases = reinterpret_cast<uintptr_t>(a.out) | reinterpret_cast<uintptr_t>(a.skip);
+  return !out_f32 && (bases & 31u) == 0 && a.out_ld % 16 == 0 && a.out_batch % 16 == 0;
+}
+
 template <int BN, int AMODE, bool B_MN, bool OUT_F32, bool HAS_BIAS, int EPI = kEpiPlain>
 cc_status launch_tc_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs& args, const DeviceInfo& di,
                          cudaStream_t stream, const char* what) {
@@ -21,6 +28,7 @@ cc_status launch_tc_gemm(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs&
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: shared-memory attribute: %s", what, cudaGetErrorString(e));
   args.err = di.err_word;
   args.timeout_ns = kWaitLimitNs;
+  args.vec32 = epi_vec32(args, OUT_F32);
   const int grid = std::min(args.num_tiles, di.sm_count);
   e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), S::kSmemBytes, stream, ta, tb, args);
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: launch: %s", what, cudaGetErrorString(e));
@@ -44,6 +52,7 @@ cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, Gemm
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: shared-memory attribute: %s", what, cudaGetErrorString(e));
   args.err = di.err_word;
   args.timeout_ns = kWaitLimitNs;
+  args.vec32 = epi_vec32(args, OUT_F32);
   const int pairs = std::min(args.num_tiles, di.sm_count / 2);
   e = launch_pdl(kern, dim3(2 * pairs), dim3(kGemmThreads), S::kSmemBytes, stream, ta, tb, tc ? *tc : tb, args);
   if (e != cudaSuccess) return fail(CC_ERR_CUDA, "%s: launch: %s", what, cudaGetErrorString(e));

@@ -129,6 +129,19 @@ __device__ __forceinline__ void tma_load_im2col_5d(uint32_t dst, const CUtensorM
       : "memory");
 }
 
+// 32-byte global accesses (one sector per lane); the address must be 32-byte
+// aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint4 (&v)[2]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0].x), "r"(v[0].y),
+               "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w)
+               : "memory");
+}
+__device__ __forceinline__ void ld_global_nc_v8(const void* p, uint32_t (&v)[8]) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(p));
+}
+
 // Shared -> global bulk copy (contiguous bytes; 16-byte aligned addresses and
 // a size that is a multiple of 16), tracked by the issuing thread's bulk group.
 __device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {

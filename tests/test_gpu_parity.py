@@ -131,6 +131,34 @@ def test_conv3d_zero_history_taps_skipped_per_tile(n, d, h, w):
     assert_parity(to_np(y), ref, f"conv {n,d,h,w}")
 
 
+def test_epilogue_with_16_byte_aligned_outputs():
+    # outputs (and the shortcut) 16 bytes past a 32-byte boundary: the
+    # epilogue falls back from its 32-byte accesses to 16-byte ones
+    def shifted(*shape):
+        buf = torch.empty(int(np.prod(shape)) + 8, dtype=BF16, device=DEV)
+        t = buf[8:].view(*shape)
+        assert t.data_ptr() % 32 == 16
+        return t
+
+    inp = inputs.conv_inputs(1, 2, 6, 11, 64, 48, seed=21, device=DEV)
+    wp = empty(27 * 48 * 64)
+    api.cc_conv3d_prepare(inp["w"], wp)
+    y = shifted(1, 2, 6, 11, 48)
+    api.cc_conv3d_causal(inp["x"], wp, inp["b"], y)
+    api.cc_check_device()
+    assert_parity(to_np(y), oracle.causal_conv3d(to_np(inp["x"]), to_np(inp["w"]), to_np(inp["b"])), "conv, shifted y")
+
+    r = inputs.resample_inputs(1, 2, 5, 9, 64, seed=22, device=DEV)
+    pw = prepare_resample(r["w"])
+    skip = shifted(1, 2, 5, 9, 64)
+    skip.copy_(r["skip"])
+    out = shifted(1, 2, 10, 18, 64)
+    api.cc_resample_up2_fused(r["x"], pw, r["b"], skip, out)
+    api.cc_check_device()
+    ref = oracle.resample_up2(to_np(r["x"]), to_np(r["w"]), to_np(r["b"]), to_np(r["skip"]))
+    assert_parity(to_np(out), ref, "fused resampler, shifted out and skip")
+
+
 def test_conv3d_mid_block_config_sampled():
     c = inputs.CONFIGS["mid_conv"]
     inp = inputs.make_config_inputs("mid_conv", device=DEV)
