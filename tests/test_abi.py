@@ -164,3 +164,41 @@ def test_size_limits_rejected_on_the_host(lib):
     assert lib.cc_attn_scores_exp(p, p, p, p, 1, hw, 64, 64, 64, hw, f, None) == 2
     assert b"too many output tiles" in lib.cc_last_error()
     assert lib.cc_attn_scores(p, p, p, 1, hw, 64, 64, 64, hw, None) == 2
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include "cc.h"
+#include "cc_debug.h"
+int main(void) {
+  if (cc_version() < 100) return 2;
+  /* a rejected request: no device needed, nothing launched */
+  if (cc_conv3d_causal(NULL, NULL, NULL, NULL, 1, 1, 1, 1, 64, 64, 0, NULL) != CC_ERR_INVALID) return 3;
+  if (cc_last_error()[0] == 0) return 4;
+  /* an empty request succeeds */
+  if (cc_head_out(NULL, NULL, NULL, NULL, 0, 1, 1, 1, 64, 0, NULL, 0, NULL) != CC_OK) return 5;
+  printf("ok\n");
+  return 0;
+}
+"""
+
+
+def test_headers_compile_and_link_as_plain_c(lib):
+    # the boundary is a C ABI: a C99 caller (pedantic, warnings as errors)
+    # includes the headers, links libcc.so and calls it
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    out = os.path.join(ROOT, "causal_convolution_gb300", "_build")
+    os.makedirs(out, exist_ok=True)
+    src = os.path.join(out, "abi_caller.c")
+    exe = os.path.join(out, "abi_caller")
+    with open(src, "w") as f:
+        f.write(C_CALLER)
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    src, "-L", libdir, "-lcc", f"-Wl,-rpath,{libdir}", "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
