@@ -269,10 +269,10 @@ cc_status cc_head_out(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, 
  * memory and so cannot pass a workspace -- for example a plugin inside a host
  * framework that owns every device allocation and exposes no allocator, or a
  * latency-critical loop where cudaMalloc (which may synchronise the device) is
- * not allowed. The paper has no counterpart to this entry point; it is an
- * addition of this library. g lives in a fixed 64 MiB array in the library's static
- * device memory, which every GPU that loads the library holds until the
- * process exits; this function allocates nothing.
+ * not allowed. The source pages have no counterpart to this entry point; it
+ * is an addition of this library. g lives in a fixed 64 MiB array in the
+ * library's static device memory, which every GPU that loads the library
+ * holds until the process exits; this function allocates nothing.
  *  - The first call on a device looks up the array's device address (no
  *    allocation) with that device current; make that first call before any
  *    stream capture on the device.
