@@ -196,7 +196,7 @@ class ClockSampler:
     def summary(self):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        sm, mx, reasons = [], [], set()
+        sm, mx, watts, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for s in self.samples:
             try:
@@ -204,11 +204,17 @@ class ClockSampler:
                 mx.append(float(s[1]))
             except ValueError:
                 continue
+            try:
+                watts.append(float(s[2]))
+            except ValueError:
+                pass
             for name, val in zip(names, s[3:7]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": round(statistics.median(watts), 1) if watts else None,
+                "power_w_max": round(max(watts), 1) if watts else None}
 
 
 # ---------------------------------------------------------------- workload --

@@ -36,3 +36,16 @@ def test_history_frames_are_seeded_and_shaped():
     c = inputs.history_frames(1, 64, 3, 5, seed=8)
     assert a.shape == (1, 2, 3, 5, 64) and a.dtype == torch.bfloat16 and a.is_contiguous()
     assert torch.equal(a, b) and not torch.equal(a, c)
+
+
+def test_clock_summary_reads_clocks_power_and_reasons():
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    c.samples = [["1900", "2070", "1350.5", "Not Active", "Not Active", "Not Active", "Active"],
+                 ["2070", "2070", "1200.0", "Not Active", "Not Active", "Not Active", "Not Active"],
+                 ["[N/A]", "2070", "[N/A]", "", "", "", ""]]
+    s = c.summary()
+    assert s["sm_mhz"] == 1985.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 2
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["power_w_median"] == 1275.2 and s["power_w_max"] == 1350.5
+    c.samples = []
+    assert c.summary()["reasons"] == ["unavailable"]
