@@ -152,7 +152,7 @@ E2E_READBACK_CTAS = 8
 class ClockSampler:
     """nvidia-smi samples (every 50 ms) of this GPU while the timed region runs."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
