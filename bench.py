@@ -404,10 +404,12 @@ class Workload:
 ORACLE_BATCH = (512, 1024, 2048, 8192)
 
 
-def oracle_sample_step(cpu, budget_s: float, rng):
+def oracle_sample_step(cpu, budget_s: float, rng, per_config=None):
     """Times the fp64 oracle on a bounded sample of each stage's outputs and
     extrapolates by output count to ms per chunk. Returns (ms_per_chunk,
-    seconds spent, description)."""
+    seconds spent, description). With a dict `per_config`, each stage's
+    figures go into it: seconds per chunk (extrapolated), outputs sampled,
+    outputs in the configuration, the sampled fraction and seconds spent."""
     import oracle
 
     total_ms = 0.0
@@ -421,7 +423,9 @@ def oracle_sample_step(cpu, budget_s: float, rng):
         chunk). The batch is fixed per stage, so the per-call setup is spread
         over the same number of outputs whatever the budget."""
         npts, dt = 0, 0.0
-        while npts == 0 or dt < per_stage:
+        # until the stage's share of the budget is spent, or as many outputs
+        # as the configuration has were timed
+        while npts == 0 or (dt < per_stage and npts < total):
             t0 = time.perf_counter()
             fn(batch)
             dt += time.perf_counter() - t0
@@ -451,7 +455,27 @@ def oracle_sample_step(cpu, budget_s: float, rng):
         spent += dt
         total_ms += ms
         desc.append(f"{name}: {npts} of {total} outputs in batches of {batch}")
+        if per_config is not None:
+            per_config[name] = {"seconds_per_chunk": round(ms * 1e-3, 3), "outputs_sampled": npts,
+                                "outputs_per_chunk": total, "fraction_sampled": round(npts / total, 6),
+                                "seconds_spent": round(dt, 3)}
     return total_ms, spent, "; ".join(desc) + " (extrapolated by output count)"
+
+
+def oracle_toy_resampler(per_config):
+    """The toy resampler configuration through the fp64 oracle in full (it
+    finishes in well under a second): wall-clock seconds, nothing sampled."""
+    import oracle
+
+    i = cc_inputs.make_config_inputs("toy_resampler", "cpu")
+    f = lambda t: t.double().numpy()
+    args = (f(i["x"]), f(i["w"]), f(i["b"]), f(i["skip"]))
+    t0 = time.perf_counter()
+    out = oracle.resample_up2(*args)
+    dt = time.perf_counter() - t0
+    per_config["toy_resampler"] = {"seconds_per_chunk": round(dt, 4), "outputs_sampled": int(out.size // out.shape[-1]),
+                                   "outputs_per_chunk": int(out.size // out.shape[-1]), "fraction_sampled": 1.0,
+                                   "seconds_spent": round(dt, 4)}
 
 
 def _pts(rng, p, n, d, h, w):
@@ -476,6 +500,8 @@ def host_inputs(device, head_frames=3):
 
 
 def cpu_threads():
+    """Threads the oracle's numpy matmuls run on (the BLAS pool), else the
+    host's CPU count."""
     try:
         from threadpoolctl import threadpool_info
         n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
@@ -483,7 +509,23 @@ def cpu_threads():
             return int(max(n))
     except Exception:
         pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        try:
+            return int(os.environ[var])
+        except (KeyError, ValueError):
+            pass
     return os.cpu_count() or 1
+
+
+def host_facts():
+    """nproc (CPUs this process may run on), the host's CPU count and the
+    thread counts the oracle's libraries are set to use."""
+    try:
+        nproc = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        nproc = os.cpu_count() or 1
+    return {"nproc": nproc, "cpu_count": os.cpu_count(), "blas_threads": cpu_threads(),
+            "omp_num_threads": os.environ.get("OMP_NUM_THREADS")}
 
 
 # -------------------------------------------------------------------- main --
@@ -523,12 +565,14 @@ def run_reference(args):
     for _ in range(args.warmup):
         oracle_sample_step(cpu, step_s, rng)
     vals, spent, desc = [], 0.0, ""
+    per_config = {}
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        v, s, desc = oracle_sample_step(cpu, step_s, rng)
+        v, s, desc = oracle_sample_step(cpu, step_s, rng, per_config)
         vals.append(v)
         spent += s
     wall = time.perf_counter() - t0
+    oracle_toy_resampler(per_config)
     value = float(np.mean(vals)) / max(args.gpus, 1)
     cores = cpu_threads()
     line = {"metric": METRIC, "value": value, "unit": "ms", "n_gpus": args.gpus, "steps": args.steps,
@@ -536,7 +580,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(args.gpus), "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle",
-                             "sample": f"per step: {desc}; fp64 numpy oracle on {cores} host threads"},
+                             "sample": f"per step: {desc}; fp64 numpy oracle on {cores} host threads",
+                             "per_config_last_step": per_config, **host_facts()},
             "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -710,9 +755,12 @@ def main(argv=None):
 
     if rank == 0 and not args.no_cpu_baseline:
         cpu = host_inputs(device)
-        v, spent, desc = oracle_sample_step(cpu, args.cpu_budget_s, np.random.default_rng(0))
+        per_config = {}
+        v, spent, desc = oracle_sample_step(cpu, args.cpu_budget_s, np.random.default_rng(0), per_config)
+        oracle_toy_resampler(per_config)
         line["cpu_baseline"] = {"value": round(v, 1), "unit": "ms", "cores": cpu_threads(), "kind": "oracle",
-                                "sample": f"{desc}; {spent:.1f} s of fp64 numpy oracle work"}
+                                "sample": f"{desc}; {spent:.1f} s of fp64 numpy oracle work",
+                                "per_config": per_config, **host_facts()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

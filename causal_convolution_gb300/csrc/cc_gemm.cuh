@@ -114,10 +114,15 @@ __device__ __forceinline__ void gemm_decode_tile(const GemmArgs& a, int tile, in
 // StoreF32: fp32 rows leave in 32-column chunks through a swizzled shared
 // staging buffer and TMA tensor stores (pair kernel only).
 // ExpBf16 (pair kernel only): the tile holds scores s of one row against BN
-// keys; per row, with c_t = ceil(exp_k * max over the tile's valid keys),
-// e = exp2(exp_k * s - c_t) in (0, 1] leaves as bf16 through the same staged
+// keys; per row, with c_t = kExpGrain * ceil(exp_k * max over the tile's valid
+// keys / kExpGrain), e = exp2(exp_k * s - c_t) in (0, 1] leaves as bf16 through the same staged
 // TMA stores, and (c_t, l_t = sum of the fp32 e) goes to stats.
 // RowScale: plain rows multiplied by 1 / l_row, l_row = sum_t 2^(c_t - c_row) l_t.
+// Granularity (log2 units) of the key-tile exponents c_t: a power of two, so
+// the rounding is exact; 32 keeps the numerators at the row maximum within
+// (2^-32, 1], far above bf16's smallest normal (2^-126).
+constexpr float kExpGrain = 32.f;
+
 enum EpiMode : int { kEpiPlain = 0, kEpiResample = 1, kEpiStoreF32 = 2, kEpiExpBf16 = 3, kEpiRowScale = 4 };
 
 // 2^e for an integer-valued e <= 0, exactly (0 below the normal range).

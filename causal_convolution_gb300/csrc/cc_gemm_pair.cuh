@@ -310,7 +310,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             if (nb + j < args.n_total) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(r[j]));
         }
       }
-      const float ct = ceilf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * kx);
+      // c_t: the tile's scaled max rounded up to a multiple of kExpGrain, so
+      // that the tiles of one row nearly always share it and the rescale pass
+      // has little to move (every e stays in (2^-kExpGrain, 1] at the max
+      // and keeps bf16's relative precision far above the normal range)
+      const float ct =
+          ceilf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * kx * (1.f / kExpGrain)) * kExpGrain;
       float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
       for (int c = 0; c < c64_end; ++c, ++chunk) {

@@ -18,6 +18,9 @@
 //  - Two calls whose work overlaps on the GPU (different streams, or
 //    different host threads without ordering) race on the array and
 //    corrupt each other's results. Order such calls on one stream.
+//  - Its device address is looked up on the first call on each device and
+//    kept for the life of the process; a cudaDeviceReset() makes that address
+//    stale, so the entry point is not to be used on a device after a reset.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -192,9 +192,11 @@ cc_status cc_attn_frame(const cc_bf16* q, const cc_bf16* k, const cc_bf16* v, cc
  *  1. cc_attn_scores_exp keeps each 128 x 256 tile of S in TMEM and writes,
  *     per row i and key tile t = j / 256, the numerators
  *     E[f,i,j] = bf16( exp2(kx * S[f,i,j] - c_t) ), kx = scale * log2(e),
- *     c_t = ceil(kx * max of the row's S over the tile), so every E is in
- *     (0, 1]; and the row statistics (c_t, l_t), l_t = sum over the tile of
- *     the unrounded exponentials.
+ *     c_t = 32 * ceil(kx * max of the row's S over the tile / 32), so every
+ *     E is in (0, 1] and the tile's largest E is above 2^-32; and the row
+ *     statistics (c_t, l_t), l_t = sum over the tile of the unrounded
+ *     exponentials. The coarse grain makes the tiles of a row share c_t in
+ *     all but rare cases, which leaves step 2 little to move.
  *  2. cc_attn_exp_rescale puts every row on one scale: c_row = max_t c_t, and
  *     each tile with c_t < c_row is multiplied in place by the exact power of
  *     two 2^(c_t - c_row), its statistics becoming (c_row, 2^(c_t - c_row) l_t).
@@ -275,7 +277,10 @@ cc_status cc_head_out(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, 
  * holds until the process exits; this function allocates nothing.
  *  - The first call on a device looks up the array's device address (no
  *    allocation) with that device current; make that first call before any
- *    stream capture on the device.
+ *    stream capture on the device. The address is kept for the life of the
+ *    process, so after cudaDeviceReset() on a device this function must not
+ *    be called again in that process (it would hand the kernels a stale
+ *    address).
  *  - More than CC_HEAD_NOALLOC_SCRATCH_BYTES / 224 positions (N*D*H*W):
  *    CC_ERR_INVALID with a message naming the limit; nothing is launched.
  *  - All calls on a device share the array and leave their g in it; nothing

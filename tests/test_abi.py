@@ -183,7 +183,7 @@ int main(void) {
 """
 
 
-def test_headers_compile_and_link_as_plain_c(lib):
+def test_headers_compile_and_link_as_plain_c(lib, tmp_path):
     # the boundary is a C ABI: a C99 caller (pedantic, warnings as errors)
     # includes the headers, links libcc.so and calls it
     import shutil
@@ -191,10 +191,8 @@ def test_headers_compile_and_link_as_plain_c(lib):
     gcc = shutil.which("gcc")
     if gcc is None:
         pytest.skip("no C compiler")
-    out = os.path.join(ROOT, "causal_convolution_gb300", "_build")
-    os.makedirs(out, exist_ok=True)
-    src = os.path.join(out, "abi_caller.c")
-    exe = os.path.join(out, "abi_caller")
+    src = str(tmp_path / "abi_caller.c")
+    exe = str(tmp_path / "abi_caller")
     with open(src, "w") as f:
         f.write(C_CALLER)
     libdir = os.path.dirname(_lib.LIB_PATH)
