@@ -6,7 +6,7 @@ at the configured sizes, every kernel launched through the C ABI:
   mid-block causal conv 1024->1024 @ 4x44x78          (1 launch)
   attention, 4 frames x 3432 positions x C=1024       (scores, softmax, PV)
   resampler 512->512 @ 8x88x156 -> 8x176x312          (phase convs, interleave)
-  output head 256->12 @ 16x352x624                    (temporal conv, stencil)
+  output head 256->12 @ 16x352x624                    (one fused kernel)
 
 `value` is milliseconds per chunk for the whole job (with N GPUs each rank
 decodes its own chunk: value = max-over-ranks step time / N). Inputs are
@@ -41,13 +41,15 @@ WORKLOAD = ("one 4-latent-frame chunk through the four stages: causal conv 1024-
             "attention 4x3432xC1024; resampler 512->512 @ 8x88x156 -> 8x176x312; head 256->12 @ 16x352x624")
 
 # The step: every row of the hot path, with the resampler's phase convs and
-# interleave (rows a4, a5) fused into one kernel and the attention (rows
-# a6-a8) through the key-tile numerators (no fp32 S round trip).
+# interleave (rows a4, a5) fused into one kernel, the attention (rows a6-a8)
+# through the key-tile numerators (no fp32 S round trip) and the head's two
+# stages (rows a9, a10) fused into one kernel (g never leaves the chip).
 KERNELS = ["conv3d_causal", "attn_scores_exp", "attn_exp_rescale", "attn_pv_exp", "resample_up2_fused",
-           "head_temporal", "head_stencil"]
-# Rows a4, a5 and a6-a8 as the separate passes of the reference design, timed
-# in their own loop after the step (not part of the step's time).
-ROW_KERNELS = ["resample_phase_conv", "resample_interleave", "attn_scores", "attn_softmax", "attn_pv"]
+           "head_out_fused"]
+# Rows a4, a5, a6-a8 and a9, a10 as the separate passes of the reference
+# design, timed in their own loop after the step (not part of the step's time).
+ROW_KERNELS = ["resample_phase_conv", "resample_interleave", "attn_scores", "attn_softmax", "attn_pv",
+               "head_temporal", "head_stencil"]
 
 
 def real_taps(frames: int, taps_per_offset: int) -> int:
@@ -86,6 +88,8 @@ def algorithmic_work(rescale_bytes: float = 0.0):
         "resample_interleave": ("hbm", (4 + 1 + 4) * m_res * rs.c * 2.0, "byte"),
         "head_temporal": ("hbm", m_head * hd.c * 2.0 + m_head * 112 * 2.0, "byte"),
         "head_stencil": ("hbm", m_head * 112 * 2.0 + m_head * 12 * 2.0, "byte"),
+        # x read once, the 12-channel output written once; g stays on chip
+        "head_out_fused": ("hbm", m_head * hd.c * 2.0 + m_head * 12 * 2.0, "byte"),
     }
 
 
@@ -105,6 +109,7 @@ KERNEL_SOURCES = {
     "attn_pv_exp": _GEMM_SRC + ["csrc/attn.cu"],
     "resample_interleave": ["csrc/passes.cu"],
     "head_stencil": ["csrc/passes.cu"],
+    "head_out_fused": _GEMM_SRC + ["csrc/head_fused.cu"],
 }
 
 
@@ -289,8 +294,8 @@ class Workload:
             ("attn", lambda: a.cc_attn_pv_exp(self.e, self.st, self.v, self.o, stream=stream)),
             ("res", lambda: a.cc_resample_up2_fused(rx, self.res_pw, self.res_b, self.res_skip, self.res_out,
                                                     hist=hist, stream=stream)),
-            ("head", lambda: a.cc_head_temporal(hx, self.head_wp, self.g, hist=hist, stream=stream)),
-            ("head", lambda: a.cc_head_stencil(self.g, self.head_b, self.head_out, stream=stream)),
+            ("head", lambda: a.cc_head_out_fused(hx, self.head_wp, self.head_b, self.head_out, hist=hist,
+                                                 stream=stream)),
         )
 
     def step(self, stream, ev=None, hist: int = 0):
@@ -303,8 +308,9 @@ class Workload:
                 ev[j + 1].record(stream)
 
     def rows(self, stream, ev):
-        """Rows a4, a5 as two passes through the phase tensors and rows a6-a8
-        as three passes through fp32 S and bf16 P (len(ROW_KERNELS)+1 events)."""
+        """Rows a4, a5 as two passes through the phase tensors, rows a6-a8 as
+        three passes through fp32 S and bf16 P, and rows a9, a10 as two passes
+        through the bf16 g (len(ROW_KERNELS)+1 events)."""
         a = self.api
         launches = (
             lambda: a.cc_resample_phase_conv(self.res_x, self.res_pw, self.phases, stream=stream),
@@ -312,6 +318,8 @@ class Workload:
             lambda: a.cc_attn_scores(self.q, self.k, self.s, stream=stream),
             lambda: a.cc_attn_softmax(self.s, self.p, self.at.hw, self.scale, stream=stream),
             lambda: a.cc_attn_pv(self.p, self.v, self.o, self.at.hw, stream=stream),
+            lambda: a.cc_head_temporal(self.head_x, self.head_wp, self.g, stream=stream),
+            lambda: a.cc_head_stencil(self.g, self.head_b, self.head_out, stream=stream),
         )
         ev[0].record(stream)
         for j, launch in enumerate(launches):
@@ -737,7 +745,8 @@ def main(argv=None):
                      + per_kernel["attn_pv"],
                      "resampler": per_kernel["resample_up2_fused"],
                      "resampler_two_pass": per_kernel["resample_phase_conv"] + per_kernel["resample_interleave"],
-                     "head": per_kernel["head_temporal"] + per_kernel["head_stencil"]},
+                     "head": per_kernel["head_out_fused"],
+                     "head_two_pass": per_kernel["head_temporal"] + per_kernel["head_stencil"]},
         "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
                     for n, r in roofs.items()},
         "traffic_source": "profiles/ncu_traffic.json (per-launch dram read+write of one ncu capture; null when the "

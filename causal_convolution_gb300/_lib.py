@@ -50,6 +50,7 @@ SIGNATURES = {
     "cc_head_stencil": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "cc_head_out": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "cc_head_out_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "cc_head_out_fused": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "cc_copy_to_host": (_I, [_P, _P, _Z, _I, _P]),
     "cc_debug_im2col_tile": (_I, [_P, _P] + [_I] * 19 + [_P]),
     "cc_debug_wait_timeout": (_I, [_L, _P]),

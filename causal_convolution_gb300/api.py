@@ -23,7 +23,7 @@ __all__ = [
     "cc_attn_exp_key_tiles", "cc_attn_exp_workspace_bytes", "cc_attn_scores_exp", "cc_attn_exp_rescale",
     "cc_attn_pv_exp", "cc_attn_frame_exp",
     "cc_head_prepare", "cc_head_workspace_bytes", "cc_head_temporal", "cc_head_stencil", "cc_head_out",
-    "cc_head_out_noalloc", "HEAD_NOALLOC_SCRATCH_BYTES", "cc_copy_to_host",
+    "cc_head_out_fused", "cc_head_out_noalloc", "HEAD_NOALLOC_SCRATCH_BYTES", "cc_copy_to_host",
     "cc_debug_im2col_tile", "cc_debug_wait_timeout",
     "HEAD_COUT", "HEAD_G_CH",
 ]
@@ -320,6 +320,16 @@ def cc_head_out(x, wp, bias, out, ws, hist: int = 0, stream=None) -> None:
     _check(_lib.load().cc_head_out(_ptr(x, name="x"), _ptr(wp, name="wp"), _ptr(bias, name="bias"),
                                    _ptr(out, name="out"), n, d, h, w, cin, hist, _ptr(ws, torch.uint8, "ws"),
                                    ws.numel(), _stream(stream)))
+
+
+def cc_head_out_fused(x, wp, bias, out, hist: int = 0, stream=None) -> None:
+    """The whole head in one kernel (g kept in fp32 on chip), no workspace."""
+    n, d, h, w, c = out.shape
+    cin = x.shape[-1]
+    if c != HEAD_COUT or tuple(x.shape) != (n, d + hist, h, w, cin) or bias.numel() != HEAD_COUT:
+        raise ValueError("head_out_fused: out must be [N,D,H,W,12] of x [N,D+hist,H,W,Cin]")
+    _check(_lib.load().cc_head_out_fused(_ptr(x, name="x"), _ptr(wp, name="wp"), _ptr(bias, name="bias"),
+                                         _ptr(out, name="out"), n, d, h, w, cin, hist, _stream(stream)))
 
 
 def cc_head_out_noalloc(x, wp, bias, out, hist: int = 0, stream=None) -> None:

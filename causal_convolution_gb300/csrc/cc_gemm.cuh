@@ -4,8 +4,9 @@
 //
 // One CTA per SM walks output tiles of 128 rows x BN columns. Warp 0 (one
 // lane) streams A and B k-blocks of 64 bf16 (one 128-byte swizzle row) into a
-// STAGES-deep shared-memory ring with TMA; warp 1 (one lane) issues
-// tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM accumulators; warps 2-5
+// STAGES-deep shared-memory ring with TMA; warp 1 (the whole warp runs the
+// loop, one elected lane issues) issues tcgen05.mma (M=128, N=BN, K=16) into
+// one of two TMEM accumulators; warps 2-5
 // drain the other accumulator (tcgen05.ld -> +bias -> bf16/fp32 -> global), so
 // the epilogue of tile i overlaps the main loop of tile i+1.
 //
@@ -365,7 +366,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    // The whole warp runs the loop (waits and descriptors stay warp-uniform);
+    // the elected lane issues the MMAs and the commits that track them.
+    {
       constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, BN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
@@ -377,14 +380,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, 1024);
       const uint64_t b_desc0 = B_MN ? sdesc_sw128(smem_u32(sB), 8192, 1024) : sdesc_sw128(smem_u32(sB), 16, 1024);
       for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
-        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, args.err, tlim)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, args.err, tlim))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * S::kAccCols;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(smem_u32(&full[stage]), phase, args.err, tlim)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, args.err, tlim))) {
             ok = false;
             break;
           }
@@ -395,24 +398,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // two 8-row groups of 128 bytes = 2048 bytes on.
           const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage) * (S::kABytes >> 4);
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (S::kBBytes >> 4);
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < kBlockK / kUmmaK; ++k)
-            mma_bf16(d_tmem, ad + 2 * k, bd + (B_MN ? 128 : 2) * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          mma_commit(smem_u32(&empty[stage]));
+            for (int k = 0; k < kBlockK / kUmmaK; ++k)
+              mma_bf16(d_tmem, ad + 2 * k, bd + (B_MN ? 128 : 2) * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            mma_commit(smem_u32(&empty[stage]));
+          }
+          __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&tfull[acc]));
+        if (elect_one()) mma_commit(smem_u32(&tfull[acc]));
+        __syncwarp();
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // No MMA may still be running when TMEM is released.
-      mma_commit(smem_u32(done));
+      if (elect_one()) mma_commit(smem_u32(done));
+      __syncwarp();
       (void)mbar_wait(smem_u32(done), 0, args.err, tlim);
     }
   } else {

@@ -214,7 +214,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------- MMA issuer (even CTA only) --
-    if (lane == 0 && leader) {
+    // The whole warp runs the loop (waits and descriptors stay warp-uniform);
+    // the elected lane issues the MMAs and the commits that track them.
+    if (leader) {
       constexpr uint32_t idesc = idesc_bf16_f32(2 * kBlockM, BN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
@@ -230,14 +232,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         int batch, mp, nt;
         pair_decode_tile(args, tile, batch, mp, nt);
         const int kb0 = tile_first_tap<AMODE>(args, batch, mp) * args.kb_per_tap;
-        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, args.err, tlim)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, args.err, tlim))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * S::kAccCols;
         for (int kb = kb0; kb < kblocks; ++kb) {
-          if (!mbar_wait(smem_u32(&full[stage]), phase, args.err, tlim)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, args.err, tlim))) {
             ok = false;
             break;
           }
@@ -248,23 +250,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           // two 8-row groups of 128 bytes = 2048 bytes on.
           const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage) * (S::kABytes >> 4);
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (S::kBBytes >> 4);
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < kBlockK / kUmmaK; ++k)
-            mma_bf16_pair(d_tmem, ad + 2 * k, bd + (B_MN ? 128 : 2) * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
-          mma_commit_pair_both(smem_u32(&empty[stage]));
+            for (int k = 0; k < kBlockK / kUmmaK; ++k)
+              mma_bf16_pair(d_tmem, ad + 2 * k, bd + (B_MN ? 128 : 2) * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            mma_commit_pair_both(smem_u32(&empty[stage]));
+          }
+          __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit_pair_both(smem_u32(&tfull[acc]));
+        if (elect_one()) mma_commit_pair_both(smem_u32(&tfull[acc]));
+        __syncwarp();
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      mma_commit_pair_both(smem_u32(done));
+      if (elect_one()) mma_commit_pair_both(smem_u32(done));
+      __syncwarp();
       (void)mbar_wait(smem_u32(done), 0, args.err, tlim);
     }
   } else if constexpr (EPI == kEpiExpBf16) {

@@ -70,6 +70,10 @@ cc_status encode_tiled_3d(CUtensorMap* map, const void* base, uint64_t d0, uint6
 // Rank-3 fp32 map with 128-byte swizzle, box {box0, box1, 1} (box0 * 4 <= 128).
 cc_status encode_tiled_3d_f32_sw128(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                                     uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1);
+// Rank-5 map with 128-byte swizzle, box {box0, box1, box2, 1, 1}; strides[i]
+// is the byte stride of dimension i + 1.
+cc_status encode_tiled_5d(CUtensorMap* map, const void* base, const uint64_t dims[5], const uint64_t strides[4],
+                          uint32_t box0, uint32_t box1, uint32_t box2);
 // Rank-4 map without swizzle (dense box in shared memory), box {b0, b1, b2, 1}.
 cc_status encode_tiled_4d_dense(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides[3],
                                 uint32_t box0, uint32_t box1, uint32_t box2);

@@ -23,8 +23,9 @@
 //    at output u0 re-reads the (up to two) input frames before it that
 //    output u0 needs. Whole tile pairs per CTA pair would leave the last
 //    wave a quarter full at the bench size (858 tile pairs on 76 CTA pairs).
-// Warp 0 streams A with TMA, warp 1 of the even CTA issues the MMAs, warps 2-5
-// of both CTAs drain accumulators to bf16 g. Every wait is bounded.
+// Warp 0 streams A with TMA, warp 1 of the even CTA issues the MMAs (the whole
+// warp runs the loop, one elected lane issues), warps 2-5 of both CTAs drain
+// accumulators to bf16 g. Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -189,14 +190,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------ MMA issuer --
-    if (lane == 0 && leader) {
+    // ---------------------------------------- MMA issuer (even CTA's warp) --
+    // The whole warp runs the loop (waits and descriptors stay warp-uniform);
+    // the elected lane issues the MMAs and the commits that track them.
+    if (leader) {
       constexpr uint32_t idesc = idesc_bf16_f32(2 * kBlockM, kHeadN, false);
       // descriptors of A stage 0 and weight block 0; the others differ only in
       // the start-address field (all blocks are 1024-byte aligned)
       const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, 1024);
       const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), 16, 1024);
-      bool ok = mbar_wait(smem_u32(bfull), 0, a.err, tlim);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bfull), 0, a.err, tlim));
       tc_fence_after();
       int stage = 0;
       uint32_t phase = 0;
@@ -211,7 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const int u = f - a.hist + 2 - kt;
             if (u < u0 || u >= u1 || f != first_frame(u, a.hist)) continue;
             const int q = q_base + u;
-            if (!mbar_wait(smem_u32(&tempty[q & 3]), ((q >> 2) & 1) ^ 1u, a.err, tlim)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty[q & 3]), ((q >> 2) & 1) ^ 1u, a.err, tlim))) {
               ok = false;
               break;
             }
@@ -230,23 +233,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             d_col[kt] = tmem_base + ((q_base + u) & 3) * kHeadAccCols;
           }
           for (int kb = 0; kb < CB; ++kb) {
-            if (!mbar_wait(smem_u32(&afull[stage]), phase, a.err, tlim)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&afull[stage]), phase, a.err, tlim))) {
               ok = false;
               break;
             }
             tc_fence_after();
             // K advances by 16 bf16 = 32 bytes = 2 in the descriptor's address field
             const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage) * (S::kABytes >> 4);
+            if (elect_one()) {
 #pragma unroll
-            for (int kt = 0; kt < 3; ++kt) {
-              if (!live[kt]) continue;
-              const uint64_t bd = b_desc0 + static_cast<uint64_t>((kt * CB + kb) * (S::kBBlock >> 4));
-              const uint32_t acc0 = (starts[kt] && kb == 0) ? 0u : 1u;
+              for (int kt = 0; kt < 3; ++kt) {
+                if (!live[kt]) continue;
+                const uint64_t bd = b_desc0 + static_cast<uint64_t>((kt * CB + kb) * (S::kBBlock >> 4));
+                const uint32_t acc0 = (starts[kt] && kb == 0) ? 0u : 1u;
 #pragma unroll
-              for (int k = 0; k < kBlockK / kUmmaK; ++k)
-                mma_bf16_pair(d_col[kt], ad + 2 * k, bd + 2 * k, idesc, k == 0 ? acc0 : 1u);
+                for (int k = 0; k < kBlockK / kUmmaK; ++k)
+                  mma_bf16_pair(d_col[kt], ad + 2 * k, bd + 2 * k, idesc, k == 0 ? acc0 : 1u);
+              }
+              mma_commit_pair_both(smem_u32(&aempty[stage]));
             }
-            mma_commit_pair_both(smem_u32(&aempty[stage]));
+            __syncwarp();
             if (++stage == AST) {
               stage = 0;
               phase ^= 1u;
@@ -254,11 +260,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
           if (!ok) break;
           const int u_done = f - a.hist;  // its kt = 2 frame was the last one
-          if (u_done >= u0 && u_done < u1) mma_commit_pair_both(smem_u32(&tfull[(q_base + u_done) & 3]));
+          if (u_done >= u0 && u_done < u1) {
+            if (elect_one()) mma_commit_pair_both(smem_u32(&tfull[(q_base + u_done) & 3]));
+            __syncwarp();
+          }
         }
         q_base += u1;
       }
-      mma_commit_pair_both(smem_u32(done));
+      if (elect_one()) mma_commit_pair_both(smem_u32(done));
+      __syncwarp();
       (void)mbar_wait(smem_u32(done), 0, a.err, tlim);
     }
   } else {

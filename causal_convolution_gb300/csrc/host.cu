@@ -163,6 +163,18 @@ cc_status encode_tiled_3d_f32_sw128(CUtensorMap* map, const void* base, uint64_t
                        "3-D fp32 map");
 }
 
+cc_status encode_tiled_5d(CUtensorMap* map, const void* base, const uint64_t dims[5], const uint64_t strides[4],
+                          uint32_t box0, uint32_t box1, uint32_t box2) {
+  const cuuint64_t d[5] = {dims[0], dims[1], dims[2], dims[3], dims[4]};
+  const cuuint64_t st[4] = {strides[0], strides[1], strides[2], strides[3]};
+  const cuuint32_t box[5] = {box0, box1, box2, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return encode_result(g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), d, st, box,
+                                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                       "5-D map");
+}
+
 cc_status encode_tiled_4d_dense(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides[3],
                                 uint32_t box0, uint32_t box1, uint32_t box2) {
   const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};

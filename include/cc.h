@@ -263,6 +263,20 @@ cc_status cc_head_stencil(const cc_bf16* g, const cc_bf16* bias, cc_bf16* out, i
 cc_status cc_head_out(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* out, int n, int d, int h,
                       int w, int cin, int hist, void* ws, size_t ws_bytes, void* stream);
 
+/* The whole head in ONE kernel, no workspace: the same result as
+ * cc_head_out (causal conv_out 3x3x3 C_in -> 12, bias, clamp to [-1, 1]) with
+ * [HEAD]'s regrouping done on chip. g (the 3x1x1 conv into 9 x 12 channels)
+ * stays in fp32 in tensor memory and registers, the 3x3 stencil sums it there,
+ * and only the output is rounded to bf16 (cc_head_out also rounds g to bf16).
+ * A CTA owns 4-row x 32-column blocks (30 interior columns plus one recomputed
+ * halo column on each side) and walks down a strip of the plane, carrying the
+ * stencil's partial sums of the rows it cannot finish yet. More than 16
+ * output frames run as several passes of at most 16 frames. x: [N, D+hist, H,
+ * W, C_in], C_in one of 64, 128, 192, 256; wp from cc_head_prepare; out:
+ * [N, D, H, W, 12]. */
+cc_status cc_head_out_fused(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* out, int n, int d,
+                            int h, int w, int cin, int hist, void* stream);
+
 /* Size of the library's built-in scratch for cc_head_out_noalloc: 64 MiB,
  * i.e. at most 64 MiB / (112 * 2 B) = 299,593 output positions per call. */
 #define CC_HEAD_NOALLOC_SCRATCH_BYTES (64u << 20)
