@@ -145,7 +145,9 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 using namespace cc;
 
-extern "C" int64_t cc_attn_ld(int hw) { return hw <= 0 ? 0 : (int64_t)round_up((size_t)hw, 8); }
+// Rows of S, P and E start on 32-byte boundaries (16 bf16 or 8 fp32 columns),
+// so the numerators' epilogue can write whole 32-byte sectors.
+extern "C" int64_t cc_attn_ld(int hw) { return hw <= 0 ? 0 : (int64_t)round_up((size_t)hw, 16); }
 
 extern "C" size_t cc_attn_workspace_bytes(int t, int hw) {
   if (t <= 0 || hw <= 0) return 0;
@@ -288,7 +290,7 @@ namespace {
 constexpr int kKeyTile = 256;  // keys per statistics tile = the scores kernel's BN
 constexpr int kRescaleWarps = 8;
 
-// One warp per row: c_row = max_t c_t; every key tile with c_t < c_row is
+// Rescale of one row by the whole warp: every key tile with c_t < c_row is
 // multiplied in place by 2^(c_t - c_row), an exact power of two (lane j takes
 // keys 8j .. 8j+7 of the tile, one 16-byte vector), and its statistics become
 // (c_row, 2^(c_t - c_row) l_t). Tiles already at c_row are not touched. Lane
@@ -296,22 +298,8 @@ constexpr int kRescaleWarps = 8;
 // once and up to kRescaleBatch of them are loaded before any is written.
 constexpr int kRescaleBatch = 8;
 
-__global__ void __launch_bounds__(kRescaleWarps * 32) exp_rescale_kernel(__nv_bfloat16* __restrict__ e,
-                                                                          float2* __restrict__ stats,
-                                                                          long long rows, int hw, long long ld_e,
-                                                                          int tiles) {
-  // launched after the scores kernel that writes e and stats; many blocks per
-  // SM, so it does not let the next kernel in early (its CTAs would take SMs
-  // this grid's later blocks still need)
-  pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * kRescaleWarps + warp;
-  if (row >= rows) return;
-  float2* st = stats + row * tiles;
-  float c_row = __int_as_float(0xff800000u);
-  for (int t = lane; t < tiles; t += 32) c_row = fmaxf(c_row, st[t].x);
-  c_row = warp_max(c_row);
-  __nv_bfloat16* er = e + row * ld_e;
+__device__ void rescale_row(__nv_bfloat16* __restrict__ er, float2* __restrict__ st, int hw, int tiles, float c_row,
+                            int lane) {
   for (int t0 = 0; t0 < tiles; t0 += 32) {
     const int tl = t0 + lane;
     const float2 mine = tl < tiles ? st[tl] : make_float2(c_row, 0.f);
@@ -348,6 +336,44 @@ __global__ void __launch_bounds__(kRescaleWarps * 32) exp_rescale_kernel(__nv_bf
         }
       }
     }
+  }
+}
+
+// One warp per 32 rows: lane l checks row r0 + l (c_row = max_t c_t over its
+// statistics, all loads in flight at once), and the warp rescales together
+// the rows that hold a tile below their c_row -- with key-tile exponents on
+// a grain of 32 those are rare, so the pass is mostly one read of the
+// statistics.
+__global__ void __launch_bounds__(kRescaleWarps * 32) exp_rescale_kernel(__nv_bfloat16* __restrict__ e,
+                                                                          float2* __restrict__ stats,
+                                                                          long long rows, int hw, long long ld_e,
+                                                                          int tiles) {
+  // launched after the scores kernel that writes e and stats; many blocks per
+  // SM, so it does not let the next kernel in early (its CTAs would take SMs
+  // this grid's later blocks still need)
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long r0 = ((long long)blockIdx.x * kRescaleWarps + warp) * 32;
+  if (r0 >= rows) return;
+  const long long row = r0 + lane;
+  float c_row = __int_as_float(0xff800000u);  // -inf
+  bool need = false;
+  if (row < rows) {
+    const float2* st = stats + row * tiles;
+    float c_min = __int_as_float(0x7f800000u);  // +inf
+    for (int t = 0; t < tiles; ++t) {
+      const float c = st[t].x;
+      c_row = fmaxf(c_row, c);
+      c_min = fminf(c_min, c);
+    }
+    need = c_min != c_row;
+  }
+  unsigned todo = __ballot_sync(0xffffffffu, need);
+  while (todo) {
+    const int l = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const float c = __shfl_sync(0xffffffffu, c_row, l);
+    rescale_row(e + (r0 + l) * ld_e, stats + (r0 + l) * tiles, hw, tiles, c, lane);
   }
 }
 }  // namespace
@@ -411,7 +437,7 @@ extern "C" cc_status cc_attn_exp_rescale(cc_bf16* e, float* stats, int t, int hw
   DeviceInfo di;
   if ((st = device_info(&di)) != CC_OK) return st;
   const long long rows = (long long)t * hw;
-  const unsigned grid = (unsigned)((rows + kRescaleWarps - 1) / kRescaleWarps);
+  const unsigned grid = (unsigned)((rows + 32LL * kRescaleWarps - 1) / (32LL * kRescaleWarps));
   const cudaError_t err = launch_pdl(exp_rescale_kernel, dim3(grid), dim3(kRescaleWarps * 32), 0,
                                      static_cast<cudaStream_t>(stream), reinterpret_cast<__nv_bfloat16*>(e),
                                      reinterpret_cast<float2*>(stats), rows, hw, (long long)ld_e,

@@ -351,19 +351,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           __nv_bfloat162 b = __floats2bfloat162_rn(e0, e1);
           pk[j] = *reinterpret_cast<uint32_t*>(&b);
         }
-        uint8_t* buf = sStage + (chunk & 1) * kStoreBufBytes;
-        if (issuer) bulk_wait_read_1();  // the store two chunks back has read this buffer
-        named_barrier_sync(1, 128);
-        uint8_t* rowp = buf + row * 128;
+        if (args.vec32) {
+          // rows start on 32-byte boundaries: each 16-key piece leaves the
+          // registers as one whole 32-byte sector, and shared memory -- whose
+          // bandwidth the main loop's operand traffic already uses up -- is
+          // not touched
+          const int m = m0 + row;
+          if (m < args.m_total) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out) + batch * args.out_batch +
+                                 static_cast<long long>(m) * args.out_ld + nb;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(rowp + ((j ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
-        if (issuer) {
-          tma_store_3d(&tmC, smem_u32(buf), nb, m0, batch);
-          bulk_commit();
+            for (int p = 0; p < 4; ++p) {
+              if (nb + 16 * p + 16 <= args.n_total) {
+                const uint4 v[2] = {make_uint4(pk[8 * p], pk[8 * p + 1], pk[8 * p + 2], pk[8 * p + 3]),
+                                    make_uint4(pk[8 * p + 4], pk[8 * p + 5], pk[8 * p + 6], pk[8 * p + 7])};
+                st_global_v8(dst + 16 * p, v);
+              } else {
+                uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const int e = 16 * p + j;
+                  if (nb + e < args.n_total) d16[e] = static_cast<uint16_t>(pk[e >> 1] >> ((e & 1) * 16));
+                }
+              }
+            }
+          }
+        } else {
+          uint8_t* buf = sStage + (chunk & 1) * kStoreBufBytes;
+          if (issuer) bulk_wait_read_1();  // the store two chunks back has read this buffer
+          named_barrier_sync(1, 128);
+          uint8_t* rowp = buf + row * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(rowp + ((j ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          fence_proxy_async_smem();
+          named_barrier_sync(1, 128);
+          if (issuer) {
+            tma_store_3d(&tmC, smem_u32(buf), nb, m0, batch);
+            bulk_commit();
+          }
         }
       }
       const float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);

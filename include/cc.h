@@ -155,7 +155,9 @@ cc_status cc_resample_up2_fused(const cc_bf16* x, const cc_bf16* pw, const cc_bf
 
 /* ------------------------------------------------ per-frame attention [ATTN] */
 
-/* Row stride (elements) used for S (fp32) and P (bf16) inside the workspace. */
+/* Row stride (elements) used for S (fp32), P and E (bf16) inside the
+ * workspaces: HW rounded up to a multiple of 16, so rows start on 32-byte
+ * boundaries. */
 int64_t cc_attn_ld(int hw);
 
 /* Bytes of workspace cc_attn_frame needs: S fp32 and P bf16, T*HW rows each. */

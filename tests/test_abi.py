@@ -60,9 +60,10 @@ def test_version_and_workspace_arithmetic(lib):
     assert lib.cc_version() >= 100
     assert lib.cc_resample_workspace_bytes(1, 8, 88, 156, 512) == 4 * 8 * 88 * 156 * 512 * 2
     assert lib.cc_head_workspace_bytes(1, 16, 352, 624) == 16 * 352 * 624 * 112 * 2
-    assert lib.cc_attn_ld(3432) == 3432
-    assert lib.cc_attn_ld(3433) == 3440
-    ld = 3432
+    assert lib.cc_attn_ld(3432) == 3440
+    assert lib.cc_attn_ld(3440) == 3440
+    assert lib.cc_attn_ld(3441) == 3456
+    ld = 3440
     assert lib.cc_attn_workspace_bytes(4, 3432) == 4 * 3432 * ld * 4 + 4 * 3432 * ld * 2
     assert lib.cc_resample_workspace_bytes(0, 1, 1, 1, 1) == 0
     assert lib.cc_attn_exp_key_tiles(3432) == 14
