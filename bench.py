@@ -227,7 +227,12 @@ class ClockSampler:
 class Workload:
     """All inputs, prepared weights, workspaces and outputs of one chunk, on one GPU."""
 
-    def __init__(self, device):
+    STAGE_OF = {"conv3d_causal": "conv", "attn_scores_exp": "attn", "attn_exp_rescale": "attn", "attn_pv_exp": "attn",
+                "resample_up2_fused": "res", "head_out_fused": "head", "resample_phase_conv": "res",
+                "resample_interleave": "res", "attn_scores": "attn", "attn_softmax": "attn", "attn_pv": "attn",
+                "head_temporal": "head", "head_stencil": "head"}
+
+    def __init__(self, device, stages=("conv", "attn", "res", "head"), history=True):
         from causal_convolution_gb300 import api
         self.api = api
         self.dev = device
@@ -236,49 +241,51 @@ class Workload:
         mk = cc_inputs.make_config_inputs
 
         cv = cc_inputs.CONFIGS["mid_conv"]
-        i = mk("mid_conv", device)
-        self.cv = cv
-        self.conv_x, self.conv_b = i["x"], i["b"]
-        self.conv_wp = E(27 * cv.cout * cv.c)
-        api.cc_conv3d_prepare(i["w"], self.conv_wp)
-        self.conv_y = E(cv.n, cv.d, cv.h, cv.w, cv.cout)
-
         at = cc_inputs.CONFIGS["attention"]
-        i = mk("attention", device)
-        self.at = at
-        self.q, self.k, self.v = i["q"], i["k"], i["v"]
-        self.ld = api.cc_attn_ld(at.hw)
-        self.s = E(at.d, at.hw, self.ld, dt=torch.float32)
-        self.p = E(at.d, at.hw, self.ld)
-        self.o = E(at.d, at.hw, at.c)
-        self.scale = at.c ** -0.5
-        self.e = E(at.d, at.hw, self.ld)
-        self.st = E(at.d, at.hw, api.cc_attn_exp_key_tiles(at.hw), 2, dt=torch.float32)
-
         rs = cc_inputs.CONFIGS["resampler"]
-        i = mk("resampler", device)
-        self.rs = rs
-        self.res_x, self.res_b, self.res_skip = i["x"], i["b"], i["skip"]
-        self.res_pw = E(48 * rs.cout * rs.c)
-        api.cc_resample_prepare(i["w"], self.res_pw)
-        self.phases = E(4, rs.n, rs.d, rs.h, rs.w, rs.cout)
-        self.res_out = E(rs.n, rs.d, 2 * rs.h, 2 * rs.w, rs.cout)
-
         hd = cc_inputs.CONFIGS["head"]
-        i = mk("head", device)
-        self.hd = hd
-        self.head_x, self.head_b = i["x"], i["b"]
-        self.head_wp = E(3 * api.HEAD_G_CH * hd.c)
-        api.cc_head_prepare(i["w"], self.head_wp)
-        self.g = E(hd.n, hd.d, hd.h, hd.w, api.HEAD_G_CH)
-        self.head_out = E(hd.n, hd.d, hd.h, hd.w, api.HEAD_COUT)
+        self.cv, self.at, self.rs, self.hd = cv, at, rs, hd
+        self.scale = at.c ** -0.5
+        hf = cc_inputs.history_frames
+        if "conv" in stages:
+            i = mk("mid_conv", device)
+            self.conv_x, self.conv_b = i["x"], i["b"]
+            self.conv_wp = E(27 * cv.cout * cv.c)
+            api.cc_conv3d_prepare(i["w"], self.conv_wp)
+            self.conv_y = E(cv.n, cv.d, cv.h, cv.w, cv.cout)
+
+        if "attn" in stages:
+            i = mk("attention", device)
+            self.q, self.k, self.v = i["q"], i["k"], i["v"]
+            self.ld = api.cc_attn_ld(at.hw)
+            self.s = E(at.d, at.hw, self.ld, dt=torch.float32)
+            self.p = E(at.d, at.hw, self.ld)
+            self.o = E(at.d, at.hw, at.c)
+            self.e = E(at.d, at.hw, self.ld)
+            self.st = E(at.d, at.hw, api.cc_attn_exp_key_tiles(at.hw), 2, dt=torch.float32)
+
+        if "res" in stages:
+            i = mk("resampler", device)
+            self.res_x, self.res_b, self.res_skip = i["x"], i["b"], i["skip"]
+            self.res_pw = E(48 * rs.cout * rs.c)
+            api.cc_resample_prepare(i["w"], self.res_pw)
+            self.phases = E(4, rs.n, rs.d, rs.h, rs.w, rs.cout)
+            self.res_out = E(rs.n, rs.d, 2 * rs.h, 2 * rs.w, rs.cout)
+
+        if "head" in stages:
+            i = mk("head", device)
+            self.head_x, self.head_b = i["x"], i["b"]
+            self.head_wp = E(3 * api.HEAD_G_CH * hd.c)
+            api.cc_head_prepare(i["w"], self.head_wp)
+            self.g = E(hd.n, hd.d, hd.h, hd.w, api.HEAD_G_CH)
+            self.head_out = E(hd.n, hd.d, hd.h, hd.w, api.HEAD_COUT)
 
         # a later chunk of a streamed decode: the causal stages get the previous
         # chunk's last two input frames in front (hist = 2) instead of zeros
-        hf = cc_inputs.history_frames
-        self.conv_xh = torch.cat([hf(cv.n, cv.c, cv.h, cv.w, 101, device), self.conv_x], 1)
-        self.res_xh = torch.cat([hf(rs.n, rs.c, rs.h, rs.w, 102, device), self.res_x], 1)
-        self.head_xh = torch.cat([hf(hd.n, hd.c, hd.h, hd.w, 104, device), self.head_x], 1)
+        if history:
+            self.conv_xh = torch.cat([hf(cv.n, cv.c, cv.h, cv.w, 101, device), self.conv_x], 1)
+            self.res_xh = torch.cat([hf(rs.n, rs.c, rs.h, rs.w, 102, device), self.res_x], 1)
+            self.head_xh = torch.cat([hf(hd.n, hd.c, hd.h, hd.w, 104, device), self.head_x], 1)
         torch.cuda.synchronize(device)
         api.cc_check_device()
 
@@ -286,7 +293,8 @@ class Workload:
         """The hot path as (stage, launch) pairs in launch order, one per entry
         of KERNELS; hist = 2 feeds the causal stages two carried history frames."""
         a = self.api
-        cx, rx, hx = (self.conv_xh, self.res_xh, self.head_xh) if hist else (self.conv_x, self.res_x, self.head_x)
+        pick = lambda name: getattr(self, name + ("h" if hist else ""), None)
+        cx, rx, hx = pick("conv_x"), pick("res_x"), pick("head_x")
         return (
             ("conv", lambda: a.cc_conv3d_causal(cx, self.conv_wp, self.conv_b, self.conv_y, hist=hist, stream=stream)),
             ("attn", lambda: a.cc_attn_scores_exp(self.q, self.k, self.e, self.st, self.scale, stream=stream)),
@@ -307,12 +315,12 @@ class Workload:
             if ev is not None:
                 ev[j + 1].record(stream)
 
-    def rows(self, stream, ev):
+    def row_launches(self, stream):
         """Rows a4, a5 as two passes through the phase tensors, rows a6-a8 as
         three passes through fp32 S and bf16 P, and rows a9, a10 as two passes
-        through the bf16 g (len(ROW_KERNELS)+1 events)."""
+        through the bf16 g, one launch per entry of ROW_KERNELS."""
         a = self.api
-        launches = (
+        return (
             lambda: a.cc_resample_phase_conv(self.res_x, self.res_pw, self.phases, stream=stream),
             lambda: a.cc_resample_interleave(self.phases, self.res_b, self.res_skip, self.res_out, stream=stream),
             lambda: a.cc_attn_scores(self.q, self.k, self.s, stream=stream),
@@ -321,6 +329,10 @@ class Workload:
             lambda: a.cc_head_temporal(self.head_x, self.head_wp, self.g, stream=stream),
             lambda: a.cc_head_stencil(self.g, self.head_b, self.head_out, stream=stream),
         )
+
+    def rows(self, stream, ev):
+        """The ROW_KERNELS launches, each bracketed by events (len(ROW_KERNELS)+1)."""
+        launches = self.row_launches(stream)
         ev[0].record(stream)
         for j, launch in enumerate(launches):
             launch()
@@ -595,6 +607,36 @@ def run_reference(args):
     return 0
 
 
+def run_profile_kernel(args):
+    """One kernel of the step on its bench workload, nothing else launched
+    after the set-up: `ncu -k regex:<kernel> -s <warmup> -c 1` then captures
+    exactly one launch."""
+    torch.cuda.set_device(0)
+    device = torch.device("cuda:0")
+    from causal_convolution_gb300 import _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        from causal_convolution_gb300 import build
+        build.build()
+    wl = Workload(device, stages=(Workload.STAGE_OF[args.profile_kernel],), history=False)
+    stream = torch.cuda.Stream(device)
+    names = KERNELS + ROW_KERNELS
+    launches = [launch for _, launch in wl.launches(stream)] + list(wl.row_launches(stream))
+    launch = launches[names.index(args.profile_kernel)]
+    if args.profile_kernel == "attn_pv_exp":  # its inputs: E and statistics from the scores kernel
+        wl.api.cc_attn_scores_exp(wl.q, wl.k, wl.e, wl.st, wl.scale, stream=stream)
+        wl.api.cc_attn_exp_rescale(wl.e, wl.st, wl.at.hw, stream=stream)
+    elif args.profile_kernel == "attn_pv":
+        wl.api.cc_attn_scores(wl.q, wl.k, wl.s, stream=stream)
+        wl.api.cc_attn_softmax(wl.s, wl.p, wl.at.hw, wl.scale, stream=stream)
+    torch.cuda.synchronize(device)
+    for _ in range(args.warmup + args.steps):
+        launch()
+    torch.cuda.synchronize(device)
+    wl.api.cc_check_device()
+    print(f"profile-kernel {args.profile_kernel}: {args.warmup + args.steps} launches", flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -606,11 +648,16 @@ def main(argv=None):
     ap.add_argument("--ref-step-s", type=float, default=4.0)
     ap.add_argument("--ref-total-s", type=float, default=150.0)
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--profile-kernel", choices=KERNELS + ROW_KERNELS, default=None,
+                    help="launch only this kernel of the step, warmup + steps times, and print nothing else "
+                         "(the target of one-kernel ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_kernel:
+        return run_profile_kernel(args)
 
     ws, rank, local = dist_setup()
     if ws > 1:
