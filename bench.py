@@ -49,7 +49,7 @@ KERNELS = ["conv3d_causal", "attn_scores_exp", "attn_exp_rescale", "attn_pv_exp"
 # Rows a4, a5, a6-a8 and a9, a10 as the separate passes of the reference
 # design, timed in their own loop after the step (not part of the step's time).
 ROW_KERNELS = ["resample_phase_conv", "resample_interleave", "attn_scores", "attn_softmax", "attn_pv",
-               "head_temporal", "head_stencil"]
+               "head_temporal", "head_stencil", "attn_frame_fused"]
 
 
 def real_taps(frames: int, taps_per_offset: int) -> int:
@@ -90,6 +90,8 @@ def algorithmic_work(rescale_bytes: float = 0.0):
         "head_stencil": ("hbm", m_head * 112 * 2.0 + m_head * 12 * 2.0, "byte"),
         # x read once, the 12-channel output written once; g stays on chip
         "head_out_fused": ("hbm", m_head * hd.c * 2.0 + m_head * 12 * 2.0, "byte"),
+        # the attention's useful products (its S is computed C/256 + 1 times)
+        "attn_frame_fused": ("tensor", 4.0 * t * hw * hw * c, "flop"),
     }
 
 
@@ -110,6 +112,7 @@ KERNEL_SOURCES = {
     "resample_interleave": ["csrc/passes.cu"],
     "head_stencil": ["csrc/passes.cu"],
     "head_out_fused": _GEMM_SRC + ["csrc/head_fused.cu"],
+    "attn_frame_fused": _GEMM_SRC + ["csrc/attn.cu", "csrc/attn_fused.cu"],
 }
 
 
@@ -230,7 +233,7 @@ class Workload:
     STAGE_OF = {"conv3d_causal": "conv", "attn_scores_exp": "attn", "attn_exp_rescale": "attn", "attn_pv_exp": "attn",
                 "resample_up2_fused": "res", "head_out_fused": "head", "resample_phase_conv": "res",
                 "resample_interleave": "res", "attn_scores": "attn", "attn_softmax": "attn", "attn_pv": "attn",
-                "head_temporal": "head", "head_stencil": "head"}
+                "head_temporal": "head", "head_stencil": "head", "attn_frame_fused": "attn"}
 
     def __init__(self, device, stages=("conv", "attn", "res", "head"), history=True):
         from causal_convolution_gb300 import api
@@ -263,6 +266,7 @@ class Workload:
             self.o = E(at.d, at.hw, at.c)
             self.e = E(at.d, at.hw, self.ld)
             self.st = E(at.d, at.hw, api.cc_attn_exp_key_tiles(at.hw), 2, dt=torch.float32)
+            self.fws = E(api.cc_attn_fused_workspace_bytes(at.d, at.hw), dt=torch.uint8)
 
         if "res" in stages:
             i = mk("resampler", device)
@@ -328,6 +332,7 @@ class Workload:
             lambda: a.cc_attn_pv(self.p, self.v, self.o, self.at.hw, stream=stream),
             lambda: a.cc_head_temporal(self.head_x, self.head_wp, self.g, stream=stream),
             lambda: a.cc_head_stencil(self.g, self.head_b, self.head_out, stream=stream),
+            lambda: a.cc_attn_frame_fused(self.q, self.k, self.v, self.o, self.fws, self.scale, stream=stream),
         )
 
     def rows(self, stream, ev):
@@ -792,6 +797,7 @@ def main(argv=None):
                      + per_kernel["attn_pv"],
                      "resampler": per_kernel["resample_up2_fused"],
                      "resampler_two_pass": per_kernel["resample_phase_conv"] + per_kernel["resample_interleave"],
+                     "attention_fused": per_kernel["attn_frame_fused"],
                      "head": per_kernel["head_out_fused"],
                      "head_two_pass": per_kernel["head_temporal"] + per_kernel["head_stencil"]},
         "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}

@@ -44,6 +44,9 @@ SIGNATURES = {
     "cc_attn_exp_rescale": (_I, [_P, _P, _I, _I, _L, _P]),
     "cc_attn_pv_exp": (_I, [_P, _P, _P, _P, _I, _I, _I, _L, _L, _L, _P]),
     "cc_attn_frame_exp": (_I, [_P, _P, _P, _P, _I, _I, _I, _L, _L, _L, _L, _F, _P, _Z, _P]),
+    "cc_attn_scores_stats": (_I, [_P, _P, _P, _I, _I, _I, _L, _L, _F, _P]),
+    "cc_attn_fused_workspace_bytes": (_Z, [_I, _I]),
+    "cc_attn_frame_fused": (_I, [_P, _P, _P, _P, _I, _I, _I, _L, _L, _L, _L, _F, _P, _Z, _P]),
     "cc_head_prepare": (_I, [_P, _P, _I, _P]),
     "cc_head_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "cc_head_temporal": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),

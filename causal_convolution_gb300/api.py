@@ -23,6 +23,7 @@ __all__ = [
     "cc_attn_exp_key_tiles", "cc_attn_exp_workspace_bytes", "cc_attn_scores_exp", "cc_attn_exp_rescale",
     "cc_attn_pv_exp", "cc_attn_frame_exp",
     "cc_head_prepare", "cc_head_workspace_bytes", "cc_head_temporal", "cc_head_stencil", "cc_head_out",
+    "cc_attn_scores_stats", "cc_attn_fused_workspace_bytes", "cc_attn_frame_fused",
     "cc_head_out_fused", "cc_head_out_noalloc", "HEAD_NOALLOC_SCRATCH_BYTES", "cc_copy_to_host",
     "cc_debug_im2col_tile", "cc_debug_wait_timeout",
     "HEAD_COUT", "HEAD_G_CH",
@@ -280,6 +281,38 @@ def cc_attn_frame_exp(q, k, v, o, ws, scale: float | None = None, stream=None) -
     _check(_lib.load().cc_attn_frame_exp(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), t, hw, c, ld_q, ld_k,
                                          ld_v, ld_o, float(scale), _ptr(ws, torch.uint8, "ws"), ws.numel(),
                                          _stream(stream)))
+
+
+def cc_attn_scores_stats(q, k, stats, scale: float | None = None, stream=None) -> None:
+    """stats: fp32 [T, HW, key_tiles, 2] (pairs c_t, l_t); E is not written."""
+    t, hw, c, ld_q = _rows(q, "q")
+    _, _, _, ld_k = _rows(k, "k")
+    tiles = cc_attn_exp_key_tiles(hw)
+    if tuple(k.shape) != (t, hw, c) or tuple(stats.shape) != (t, hw, tiles, 2):
+        raise ValueError(f"attn_scores_stats: k must be [T,HW,C] and stats [T,HW,{tiles},2]")
+    if scale is None:
+        scale = c ** -0.5
+    _check(_lib.load().cc_attn_scores_stats(q.data_ptr(), k.data_ptr(), _ptr(stats, torch.float32, "stats"), t, hw,
+                                            c, ld_q, ld_k, float(scale), _stream(stream)))
+
+
+def cc_attn_fused_workspace_bytes(t: int, hw: int) -> int:
+    return _lib.load().cc_attn_fused_workspace_bytes(t, hw)
+
+
+def cc_attn_frame_fused(q, k, v, o, ws, scale: float | None = None, stream=None) -> None:
+    """Attention with the numerators kept on chip (statistics pass + one kernel)."""
+    t, hw, c, ld_q = _rows(q, "q")
+    _, _, _, ld_k = _rows(k, "k")
+    _, _, _, ld_v = _rows(v, "v")
+    _, _, _, ld_o = _rows(o, "o")
+    if not (tuple(k.shape) == tuple(v.shape) == tuple(o.shape) == (t, hw, c)):
+        raise ValueError("attn_frame_fused: q, k, v, o must share [T,HW,C]")
+    if scale is None:
+        scale = c ** -0.5
+    _check(_lib.load().cc_attn_frame_fused(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), t, hw, c, ld_q,
+                                           ld_k, ld_v, ld_o, float(scale), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                           _stream(stream)))
 
 
 # -------------------------------------------------------------- output head --

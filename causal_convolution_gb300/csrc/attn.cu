@@ -427,6 +427,42 @@ extern "C" cc_status cc_attn_scores_exp(const cc_bf16* q, const cc_bf16* k, cc_b
       ta, tb, a, di, static_cast<cudaStream_t>(stream), what, &tc);
 }
 
+extern "C" cc_status cc_attn_scores_stats(const cc_bf16* q, const cc_bf16* k, float* stats, int t, int hw, int c,
+                                          int64_t ld_q, int64_t ld_k, float scale, void* stream) {
+  const char* what = "attn_scores_stats";
+  cc_status st;
+  if (empty_request(what, {t, hw}, &st)) return st;
+  if ((st = check_ptr(what, q)) != CC_OK || (st = check_ptr(what, k)) != CC_OK ||
+      (st = check_ptr(what, stats)) != CC_OK)
+    return st;
+  if (t <= 0 || hw <= 0 || c <= 0) return fail(CC_ERR_INVALID, "%s: sizes must be positive", what);
+  if (c % 64 != 0) return fail(CC_ERR_UNSUPPORTED, "%s: C must be a multiple of 64 (got %d)", what, c);
+  if ((st = check_tiles(what, t, hw, hw)) != CC_OK) return st;
+  if (ld_q < c || ld_k < c) return fail(CC_ERR_INVALID, "%s: row strides too small", what);
+  if (ld_q % 8 || ld_k % 8) return fail(CC_ERR_INVALID, "%s: row strides must be multiples of 8", what);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CC_ERR_INVALID, "%s: scale must be finite and > 0", what);
+  DeviceInfo di;
+  if ((st = device_info(&di)) != CC_OK) return st;
+  CUtensorMap ta, tb;
+  if ((st = encode_tiled_3d(&ta, q, c, hw, t, 2ull * ld_q, 2ull * ld_q * hw, kBlockK, kBlockM)) != CC_OK) return st;
+  if ((st = encode_tiled_3d(&tb, k, c, hw, t, 2ull * ld_k, 2ull * ld_k * hw, kBlockK, 128)) != CC_OK) return st;
+  GemmArgs a{};
+  a.m_total = hw;
+  a.n_total = hw;
+  a.m_tiles = ceil_div(hw, kBlockM);
+  a.n_tiles = ceil_div(hw, kKeyTile);
+  a.batches = t;
+  a.num_tiles = a.m_tiles * a.n_tiles * t;
+  a.taps = 1;
+  a.kb_per_tap = c / kBlockK;
+  a.out = nullptr;  // the numerators' epilogue then writes the statistics only
+  a.stats = reinterpret_cast<float2*>(stats);
+  a.stat_tiles = a.n_tiles;
+  a.exp_k = scale * 1.4426950408889634f;
+  return launch_tc_gemm_pair<kKeyTile, kATiled3d, false, false, false, kEpiExpBf16>(
+      ta, tb, a, di, static_cast<cudaStream_t>(stream), what, &tb);
+}
+
 extern "C" cc_status cc_attn_exp_rescale(cc_bf16* e, float* stats, int t, int hw, int64_t ld_e, void* stream) {
   const char* what = "attn_exp_rescale";
   cc_status st;

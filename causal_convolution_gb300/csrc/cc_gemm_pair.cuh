@@ -351,7 +351,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           __nv_bfloat162 b = __floats2bfloat162_rn(e0, e1);
           pk[j] = *reinterpret_cast<uint32_t*>(&b);
         }
-        if (args.vec32) {
+        if (args.out == nullptr) {
+          // statistics only: E is not written
+        } else if (args.vec32) {
           // rows start on 32-byte boundaries: each 16-key piece leaves the
           // registers as one whole 32-byte sector, and shared memory -- whose
           // bandwidth the main loop's operand traffic already uses up -- is

@@ -236,6 +236,28 @@ cc_status cc_attn_frame_exp(const cc_bf16* q, const cc_bf16* k, const cc_bf16* v
                             int64_t ld_q, int64_t ld_k, int64_t ld_v, int64_t ld_o, float scale, void* ws,
                             size_t ws_bytes, void* stream);
 
+/* Step 1 alone, statistics only: the (c_t, l_t) of cc_attn_scores_exp for
+ * every row and key tile, E not written. stats: T*HW*cc_attn_exp_key_tiles(HW)
+ * pairs. Needs C % 64 == 0, ld_q and ld_k % 8 == 0, scale finite and > 0. */
+cc_status cc_attn_scores_stats(const cc_bf16* q, const cc_bf16* k, float* stats, int t, int hw, int c, int64_t ld_q,
+                               int64_t ld_k, float scale, void* stream);
+
+/* Attention with the numerators kept on chip ([ATTN]'s scores, row softmax
+ * and PV with nothing between them in memory): cc_attn_scores_stats, then
+ * one kernel that, per frame, 256 query rows and 256 channels of O, walks the
+ * 256-key tiles, computes S in tensor memory, turns it into
+ * E = bf16(exp2(kx * S - c_row)) in shared memory (c_row = the row's largest
+ * c_t, so no tile is rescaled) and accumulates E v into O, divided by
+ * l_row = sum_t 2^(c_t - c_row) l_t and rounded once at the end. S is
+ * computed once per 256-channel chunk of O (O for all C channels of a row
+ * block would not fit in tensor memory): C / 256 + 1 times the scores work.
+ * Same contract as cc_attn_frame with C % 256 == 0 and a workspace of
+ * cc_attn_fused_workspace_bytes() (the statistics only). */
+size_t cc_attn_fused_workspace_bytes(int t, int hw);
+cc_status cc_attn_frame_fused(const cc_bf16* q, const cc_bf16* k, const cc_bf16* v, cc_bf16* o, int t, int hw, int c,
+                              int64_t ld_q, int64_t ld_k, int64_t ld_v, int64_t ld_o, float scale, void* ws,
+                              size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------ output head [HEAD] */
 
 #define CC_HEAD_COUT 12
