@@ -74,6 +74,13 @@ struct GemmArgs {
   float2* stats;
   int stat_tiles;   // key tiles per row
   float exp_k;      // scale * log2(e): exp(scale * s) = exp2(exp_k * s)
+  // Pair kernel: when mp_perm_n > 0, the k-th 256-row pair tile in walking
+  // order is mp_perm[k] (set by the launcher for im2col convolutions over
+  // several frames: tiles at the same position inside a frame, one per
+  // frame, come one after another, so the rows a tile's temporal taps read
+  // were loaded moments before by its neighbours and are still in L2)
+  int mp_perm_n;
+  unsigned short mp_perm[512];
   unsigned int* err;
   unsigned long long timeout_ns;
 };

@@ -61,4 +61,36 @@ cc_status launch_tc_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, Gemm
 
 inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
+// Walking order of the 256-row pair tiles of an im2col convolution over
+// [N, D, H, W] positions. With zero frames before frame 0 (lo_d < 0) the
+// tiles whose rows lie in the first -lo_d frames skip their leading taps and
+// are short: they go first, in plain order (the snake then evens out their
+// cost across CTA pairs, as before). The full tiles follow, sorted by
+// (image, position of the tile's first row inside its frame, tile): the
+// tiles at one place of the plane, one per frame, follow each other, so a
+// tile's earlier-frame taps find their rows in L2 instead of DRAM. Left as
+// the identity (mp_perm_n = 0) for a single frame or more pair tiles than
+// the table holds.
+inline void set_frame_interleaved_order(GemmArgs& a) {
+  a.mp_perm_n = 0;
+  const long long mpt = (a.m_tiles + 1LL) / 2;
+  const long long plane = static_cast<long long>(a.img_h) * a.img_w;
+  const long long image = plane * a.img_d;
+  constexpr long long kMax = sizeof(a.mp_perm) / sizeof(a.mp_perm[0]);
+  if (a.img_d <= 1 || mpt <= 1 || mpt > kMax || plane <= 0) return;
+  long long key[kMax];
+  for (long long mp = 0; mp < mpt; ++mp) {
+    const long long r0 = mp * 2 * kBlockM;
+    const long long r1 = std::min(r0 + 2 * kBlockM, static_cast<long long>(a.m_total)) - 1;
+    // the latest frame a row of the tile lies in (the tile_first_tap rule)
+    const long long t_max = r0 / image != r1 / image ? a.img_d - 1 : (r1 % image) / plane;
+    const bool short_tile = a.lo_d < 0 && t_max + a.lo_d < 0;
+    const long long order = short_tile ? mp : mpt + (r0 / image) * image + (r0 % image) % plane;
+    key[mp] = order * kMax + mp;
+  }
+  std::sort(key, key + mpt);
+  for (long long i = 0; i < mpt; ++i) a.mp_perm[i] = static_cast<unsigned short>(key[i] % kMax);
+  a.mp_perm_n = static_cast<int>(mpt);
+}
+
 }  // namespace cc

@@ -48,6 +48,7 @@ __device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, in
     batch = r % a.batches;
     mp = r / a.batches;
   }
+  if (a.mp_perm_n > 0) mp = a.mp_perm[mp];
 }
 
 // Taps are ordered by their temporal offset. With zero frames before frame 0

@@ -168,6 +168,7 @@ extern "C" cc_status cc_conv3d_causal(const cc_bf16* x, const cc_bf16* wp, const
   a.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pair) {
+    set_frame_interleaved_order(a);
     if (bias) return launch_tc_gemm_pair<256, kAIm2col, false, false, true>(ta, tb, a, di, s, what);
     return launch_tc_gemm_pair<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
   }
@@ -249,7 +250,10 @@ extern "C" cc_status cc_resample_phase_conv(const cc_bf16* x, const cc_bf16* pw,
   a.out_batch = m * cout;
   a.bias = nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (pair) return launch_tc_gemm_pair<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
+  if (pair) {
+    set_frame_interleaved_order(a);
+    return launch_tc_gemm_pair<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
+  }
   return launch_tc_gemm<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
 }
 
@@ -324,6 +328,9 @@ extern "C" cc_status cc_resample_up2_fused(const cc_bf16* x, const cc_bf16* pw, 
   a.skip = reinterpret_cast<const __nv_bfloat16*>(skip);
   a.epi_tscale = temporal ? 2 : 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (pair) return launch_tc_gemm_pair<256, kAIm2col, false, false, true, kEpiResample>(ta, tb, a, di, s, what);
+  if (pair) {
+    set_frame_interleaved_order(a);
+    return launch_tc_gemm_pair<256, kAIm2col, false, false, true, kEpiResample>(ta, tb, a, di, s, what);
+  }
   return launch_tc_gemm<256, kAIm2col, false, false, true, kEpiResample>(ta, tb, a, di, s, what);
 }
