@@ -62,7 +62,7 @@ constexpr int kTC = 32;               // block columns: one lane each
 constexpr int kTI = kTC - 2;          // interior columns per strip
 constexpr int kMaxD = 16;             // output frames per pass (carried state)
 constexpr int kMaxCtas = 256;         // shares the host can hand out
-constexpr int kPrefetchFrames = 2;    // x frames requested into L2 ahead of their loads
+constexpr int kPrefetchFrames = 1;    // x frames requested into L2 ahead of their loads
 constexpr int kSmemBudget = 232448;
 
 struct FusedArgs {
