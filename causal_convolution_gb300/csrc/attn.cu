@@ -348,9 +348,11 @@ __global__ void __launch_bounds__(kRescaleWarps * 32) exp_rescale_kernel(__nv_bf
                                                                           float2* __restrict__ stats,
                                                                           long long rows, int hw, long long ld_e,
                                                                           int tiles) {
-  // launched after the scores kernel that writes e and stats; many blocks per
-  // SM, so it does not let the next kernel in early (its CTAs would take SMs
-  // this grid's later blocks still need)
+  // launched after the scores kernel that writes e and stats; the grid is one
+  // wave (32 rows per warp), so the next kernel may be scheduled at once: its
+  // CTAs take the idle SMs and do their set-up, then wait for this grid to
+  // complete before they read e
+  pdl_launch_dependents();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long r0 = ((long long)blockIdx.x * kRescaleWarps + warp) * 32;

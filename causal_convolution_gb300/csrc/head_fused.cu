@@ -578,8 +578,8 @@ extern "C" cc_status cc_head_out_fused(const cc_bf16* x, const cc_bf16* wp, cons
   if (cin <= 0 || cin % 64 != 0 || cin > 256)
     return fail(CC_ERR_UNSUPPORTED, "%s: C_in must be 64, 128, 192 or 256 (got %d)", what, cin);
   const long long strips = (w + kTI - 1) / kTI;
-  if ((long long)n * strips * h > (1LL << 40) || (long long)n * (d + hist) * h * w > (1LL << 40) ||
-      h > (1 << 30) || w > (1 << 30))
+  if ((long long)n * strips > (1LL << 30) || (long long)n * strips * h > (1LL << 40) ||
+      (long long)n * (d + hist) * h * w > (1LL << 40) || h > (1 << 30) || w > (1 << 30))
     return fail(CC_ERR_UNSUPPORTED, "%s: tensor too large", what);
   DeviceInfo di;
   if ((st = device_info(&di)) != CC_OK) return st;
