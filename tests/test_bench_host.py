@@ -49,3 +49,29 @@ def test_clock_summary_reads_clocks_power_and_reasons():
     assert s["power_w_median"] == 1275.2 and s["power_w_max"] == 1350.5
     c.samples = []
     assert c.summary()["reasons"] == ["unavailable"]
+
+
+def test_every_bench_kernel_has_work_sources_and_a_stage():
+    work = bench.algorithmic_work(rescale_bytes=1.0)
+    for name in bench.KERNELS + bench.ROW_KERNELS:
+        assert name in work and name in bench.KERNEL_SOURCES and name in bench.Workload.STAGE_OF, name
+        assert len(bench.kernel_source_hash(name)) == 64
+    assert len(set(bench.KERNELS + bench.ROW_KERNELS)) == len(bench.KERNELS) + len(bench.ROW_KERNELS)
+
+
+def test_algorithmic_work_of_the_fused_kernels():
+    work = bench.algorithmic_work(rescale_bytes=0.0)
+    hd, at = inputs.CONFIGS["head"], inputs.CONFIGS["attention"]
+    positions = hd.n * hd.d * hd.h * hd.w
+    # the fused head reads x once and writes the 12-channel output once
+    assert work["head_out_fused"] == ("hbm", positions * (256 + 12) * 2.0, "byte")
+    assert abs(work["head_out_fused"][1] / 1.884e9 - 1) < 1e-3
+    # the fused attention is credited with the attention's own products only
+    assert work["attn_frame_fused"] == ("tensor", 2 * work["attn_scores"][1], "flop")
+    assert work["attn_frame_fused"][1] == 4.0 * at.d * at.hw * at.hw * at.c
+
+
+def test_profile_kernel_accepts_only_bench_kernels():
+    import pytest
+    with pytest.raises(SystemExit):
+        bench.main(["--profile-kernel", "not_a_kernel"])
