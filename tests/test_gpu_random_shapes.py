@@ -1,5 +1,6 @@
 """Seeded random shapes through every stage -- the causal conv, the fused
-resampler (spatial and temporal), the head and the key-tile attention --
+resampler (spatial and temporal), the head (two kernels and fused), the
+key-tile attention and the fused attention --
 each checked whole against the fp64 oracle. The shapes are small enough for
 the oracle and are drawn once from a fixed generator, so a failure names a
 reproducible case: ragged tails, one-row and one-column planes, several
@@ -43,6 +44,10 @@ RESAMPLE = _cases(12, 8, lambda r: (int(r.integers(1, 3)), int(r.integers(1, 4))
 HEAD = _cases(13, 8, lambda r: (int(r.integers(1, 3)), int(r.integers(1, 5)), int(r.integers(1, 13)),
                                 int(r.integers(1, 31)), int(r.choice([64, 128, 192, 256])), int(r.choice([0, 2]))))
 ATTN = _cases(14, 8, lambda r: (int(r.integers(1, 4)), int(r.integers(1, 701)), int(r.choice([64, 128, 192, 256]))))
+HEAD_FUSED = _cases(15, 10, lambda r: (int(r.integers(1, 3)), int(r.integers(1, 20)), int(r.integers(1, 14)),
+                                       int(r.integers(1, 75)), int(r.choice([64, 128, 192, 256])),
+                                       int(r.choice([0, 2]))))
+ATTN_FUSED = _cases(16, 8, lambda r: (int(r.integers(1, 4)), int(r.integers(1, 801)), int(r.choice([256, 512]))))
 
 
 @pytest.mark.parametrize("n,d,h,w,cin,cout,hist,bias", CONV)
@@ -108,3 +113,31 @@ def test_attention_key_tiles_random_shape(t, hw, c):
     api.cc_check_device()
     ref = oracle.attn_frame(to_np(q), to_np(k), to_np(v))
     assert_parity(to_np(o), ref, f"attention {t, hw, c}")
+
+
+@pytest.mark.parametrize("n,d,h,w,cin,hist", HEAD_FUSED)
+def test_head_fused_random_shape(n, d, h, w, cin, hist):
+    g = torch.Generator(device=DEV).manual_seed(n * 1000 + d * 100 + h * 10 + w + 7)
+    x = _rnd((n, d + hist, h, w, cin), g, 2.0)
+    wt = _rnd((api.HEAD_COUT, cin, 3, 3, 3), g, (27 * cin) ** -0.5)
+    b = _rnd((api.HEAD_COUT,), g, 0.2)
+    wp = torch.empty(3 * api.HEAD_G_CH * cin, dtype=BF16, device=DEV)
+    api.cc_head_prepare(wt, wp)
+    out = torch.empty((n, d, h, w, api.HEAD_COUT), dtype=BF16, device=DEV)
+    api.cc_head_out_fused(x, wp, b, out, hist=hist)
+    api.cc_check_device()
+    xn = to_np(x)
+    ref = oracle.head_out(xn[:, hist:], to_np(wt), to_np(b), history=xn[:, :2] if hist else None)
+    assert_parity(to_np(out), ref, f"fused head {n, d, h, w, cin, hist}")
+
+
+@pytest.mark.parametrize("t,hw,c", ATTN_FUSED)
+def test_attention_fused_random_shape(t, hw, c):
+    g = torch.Generator(device=DEV).manual_seed(t * 10000 + hw * 10 + c + 3)
+    q, k, v = (_rnd((t, hw, c), g) for _ in range(3))
+    o = torch.empty((t, hw, c), dtype=BF16, device=DEV)
+    ws = torch.empty(api.cc_attn_fused_workspace_bytes(t, hw), dtype=torch.uint8, device=DEV)
+    api.cc_attn_frame_fused(q, k, v, o, ws)
+    api.cc_check_device()
+    ref = oracle.attn_frame(to_np(q), to_np(k), to_np(v))
+    assert_parity(to_np(o), ref, f"fused attention {t, hw, c}")
