@@ -89,10 +89,29 @@ def algorithmic_work(rescale_bytes: float = 0.0):
         "head_temporal": ("hbm", m_head * hd.c * 2.0 + m_head * 112 * 2.0, "byte"),
         "head_stencil": ("hbm", m_head * 112 * 2.0 + m_head * 12 * 2.0, "byte"),
         # x read once, the 12-channel output written once; g stays on chip
+        # (its multiply-adds, nearly as binding: head_tensor_work)
         "head_out_fused": ("hbm", m_head * hd.c * 2.0 + m_head * 12 * 2.0, "byte"),
         # the attention's useful products (its S is computed C/256 + 1 times)
         "attn_frame_fused": ("tensor", 4.0 * t * hw * hw * c, "flop"),
     }
+
+
+def head_tensor_work():
+    """The fused head's multiply-adds: (useful, executed) flops per launch.
+    Useful: the 12-channel 3x3x3 conv over real input frames (the products
+    with the causal zero frames are skipped, as in the convolutions).
+    Executed: what its MMAs run -- 112 accumulator columns for 108 used, and
+    each 32-column block recomputes its two halo columns (strips of 30
+    interior columns: ceil(W/30) blocks of 32 columns per row), plus one g row
+    above each strip's first block (every strip is one segment here)."""
+    hd = cc_inputs.CONFIGS["head"]
+    plane = hd.h * hd.w
+    useful = 2.0 * plane * 12 * real_taps(hd.d, 9) * hd.c
+    strips = -(-hd.w // 30)
+    blocks_rows = -(-(hd.h + 2) // 4) * 4  # g rows the blocks of one strip cover
+    # every input frame's block feeds the outputs that read it: 3 d - 3 frame pairs
+    executed = 2.0 * hd.n * (strips * 32) * blocks_rows * 112 * (3 * hd.d - 3) * hd.c
+    return useful, executed
 
 
 # The source files each kernel is built from (for tying ncu counters to code).
@@ -772,6 +791,22 @@ def main(argv=None):
             roofs[name]["traffic_gbs"] = traffic[name] / (per_kernel[name] * 1e-3) / 1e9
         if name in per_kernel_stats:
             roofs[name]["ms_median"], roofs[name]["ms_min"] = per_kernel_stats[name]
+    # the fused head against the tensor roof too: its useful multiply-adds
+    # take nearly as long at the bf16 peak as its bytes at the copy peak
+    hu, hx = head_tensor_work()
+    hsec = per_kernel["head_out_fused"] * 1e-3
+    roofs["head_out_fused"]["tensor"] = {
+        "achieved": hu / hsec / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+        "frac": hu / hsec / 1e12 / peaks["bf16_tflops"], "work": hu, "executed_work": hx,
+        "executed_frac": hx / hsec / 1e12 / peaks["bf16_tflops"]}
+    # the whole step against the tensor roof: the useful flops of its five
+    # tensor-core stages over the step's time
+    step_flops = sum(work[n][1] for n in ("conv3d_causal", "attn_scores_exp", "attn_pv_exp", "resample_up2_fused")) + hu
+    step_roof = {"useful_tflop": round(step_flops / 1e12, 4),
+                 "achieved": round(step_flops / (ms_step * 1e-3) / 1e12, 2), "peak": peaks["bf16_tflops"],
+                 "unit": "TFLOP/s", "frac": round(step_flops / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                 "what": "conv + attention scores and PV + fused resampler + fused head multiply-adds (real taps) "
+                         "per step time, against the burst bf16 peak"}
     dominant = max(KERNELS, key=lambda n: per_kernel[n])
     dr = roofs[dominant]
     roofline = {"bound": dr["bound"], "achieved": round(dr["achieved"], 2), "peak": dr["peak"], "unit": dr["unit"],
@@ -800,11 +835,15 @@ def main(argv=None):
                      "attention_fused": per_kernel["attn_frame_fused"],
                      "head": per_kernel["head_out_fused"],
                      "head_two_pass": per_kernel["head_temporal"] + per_kernel["head_stencil"]},
-        "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
+        "kernels": {n: {k: (round(v, 4) if isinstance(v, float) else
+                            {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                            if isinstance(v, dict) else v)
+                        for k, v in r.items()}
                     for n, r in roofs.items()},
         "traffic_source": "profiles/ncu_traffic.json (per-launch dram read+write of one ncu capture; null when the "
                           "kernel's sources changed since)",
         "roofline": roofline,
+        "step_roofline": step_roof,
         "steady_state": {"ms_per_step": round(steady_ms, 4),
                          "what": "the same step on a later chunk of a streamed decode: conv, resampler and head get "
                                  "the previous chunk's last two input frames (hist=2) instead of the zero frames, so "

@@ -66,6 +66,14 @@ def test_algorithmic_work_of_the_fused_kernels():
     # the fused head reads x once and writes the 12-channel output once
     assert work["head_out_fused"] == ("hbm", positions * (256 + 12) * 2.0, "byte")
     assert abs(work["head_out_fused"][1] / 1.884e9 - 1) < 1e-3
+    # its multiply-adds: the 12-channel conv over real frames (45 of 48
+    # temporal taps at 16 frames); the MMAs run 112 columns over 32-column
+    # blocks of 30 interior columns (21 per 624-column row) and 89 4-row
+    # blocks per strip
+    useful, executed = bench.head_tensor_work()
+    assert useful == 2.0 * hd.h * hd.w * 12 * 9 * (3 * hd.d - 3) * hd.c
+    assert executed == 2.0 * (21 * 32) * (89 * 4) * 112 * (3 * hd.d - 3) * hd.c
+    assert 1.12 < executed / useful < 1.14
     # the fused attention is credited with the attention's own products only
     assert work["attn_frame_fused"] == ("tensor", 2 * work["attn_scores"][1], "flop")
     assert work["attn_frame_fused"][1] == 4.0 * at.d * at.hw * at.hw * at.c
