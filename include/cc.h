@@ -314,11 +314,10 @@ cc_status cc_head_out_fused(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* 
  * library's static device memory, which every GPU that loads the library
  * holds until the process exits; this function allocates nothing.
  *  - The first call on a device looks up the array's device address (no
- *    allocation) with that device current; make that first call before any
- *    stream capture on the device. The address is kept for the life of the
- *    process, so after cudaDeviceReset() on a device this function must not
- *    be called again in that process (it would hand the kernels a stale
- *    address).
+ *    allocation) with that device current. The address is kept for the life
+ *    of the process, so after cudaDeviceReset() on a device this function
+ *    must not be called again in that process (it would hand the kernels a
+ *    stale address).
  *  - More than CC_HEAD_NOALLOC_SCRATCH_BYTES / 224 positions (N*D*H*W):
  *    CC_ERR_INVALID with a message naming the limit; nothing is launched.
  *  - All calls on a device share the array and leave their g in it; nothing

@@ -1,4 +1,4 @@
-"""The whole step -- seven launches with programmatic dependencies -- captured
+"""The whole step -- six launches with programmatic dependencies -- captured
 once into a CUDA graph and replayed: every output equals, bit for bit, that
 of the same launches issued one by one (the kernels are deterministic). The
 library makes no allocation, host synchronisation or device-wide call on its
