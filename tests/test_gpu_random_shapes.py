@@ -1,6 +1,6 @@
-"""Seeded random shapes through every stage -- the causal conv, the fused
-resampler (spatial and temporal), the head (two kernels and fused), the
-key-tile attention and the fused attention --
+"""Seeded random shapes through every stage -- the causal conv, the
+resampler (fused, spatial and temporal, and in two passes), the head (two
+kernels and fused), the attention (three passes, key tiles, fused) --
 each checked whole against the fp64 oracle. The shapes are small enough for
 the oracle and are drawn once from a fixed generator, so a failure names a
 reproducible case: ragged tails, one-row and one-column planes, several
@@ -48,6 +48,11 @@ HEAD_FUSED = _cases(15, 10, lambda r: (int(r.integers(1, 3)), int(r.integers(1, 
                                        int(r.integers(1, 75)), int(r.choice([64, 128, 192, 256])),
                                        int(r.choice([0, 2]))))
 ATTN_FUSED = _cases(16, 8, lambda r: (int(r.integers(1, 4)), int(r.integers(1, 801)), int(r.choice([256, 512]))))
+RESAMPLE_TWO_PASS = _cases(17, 6, lambda r: (int(r.integers(1, 3)), int(r.integers(1, 4)), int(r.integers(1, 11)),
+                                             int(r.integers(1, 15)), int(r.choice([64, 128])),
+                                             int(r.choice([16, 64, 96, 256])), int(r.choice([0, 2]))))
+ATTN_THREE_PASS = _cases(18, 6, lambda r: (int(r.integers(1, 4)), int(r.integers(1, 701)),
+                                           int(r.choice([64, 128, 192, 256]))))
 
 
 @pytest.mark.parametrize("n,d,h,w,cin,cout,hist,bias", CONV)
@@ -141,3 +146,33 @@ def test_attention_fused_random_shape(t, hw, c):
     api.cc_check_device()
     ref = oracle.attn_frame(to_np(q), to_np(k), to_np(v))
     assert_parity(to_np(o), ref, f"fused attention {t, hw, c}")
+
+
+@pytest.mark.parametrize("n,d,hl,wl,cin,cout,hist", RESAMPLE_TWO_PASS)
+def test_resample_two_pass_random_shape(n, d, hl, wl, cin, cout, hist):
+    g = torch.Generator(device=DEV).manual_seed(n * 1000 + d * 100 + hl * 10 + wl + 11)
+    x = _rnd((n, d + hist, hl, wl, cin), g)
+    wt = _rnd((cout, cin, 3, 3, 3), g, (27 * cin) ** -0.5)
+    b = _rnd((cout,), g, 0.1)
+    skip = _rnd((n, d, hl, wl, cout), g)
+    pw = torch.empty(48 * cout * cin, dtype=BF16, device=DEV)
+    api.cc_resample_prepare(wt, pw)
+    out = torch.empty((n, d, 2 * hl, 2 * wl, cout), dtype=BF16, device=DEV)
+    ws = torch.empty(api.cc_resample_workspace_bytes(n, d, hl, wl, cout), dtype=torch.uint8, device=DEV)
+    api.cc_resample_up2(x, pw, b, skip, out, ws, hist=hist)
+    api.cc_check_device()
+    xn = to_np(x)
+    ref = oracle.resample_up2(xn[:, hist:], to_np(wt), to_np(b), to_np(skip), history=xn[:, :2] if hist else None)
+    assert_parity(to_np(out), ref, f"two-pass resampler {n, d, hl, wl, cin, cout, hist}")
+
+
+@pytest.mark.parametrize("t,hw,c", ATTN_THREE_PASS)
+def test_attention_three_pass_random_shape(t, hw, c):
+    g = torch.Generator(device=DEV).manual_seed(t * 10000 + hw * 10 + c + 5)
+    q, k, v = (_rnd((t, hw, c), g) for _ in range(3))
+    o = torch.empty((t, hw, c), dtype=BF16, device=DEV)
+    ws = torch.empty(api.cc_attn_workspace_bytes(t, hw), dtype=torch.uint8, device=DEV)
+    api.cc_attn_frame(q, k, v, o, ws)
+    api.cc_check_device()
+    ref = oracle.attn_frame(to_np(q), to_np(k), to_np(v))
+    assert_parity(to_np(o), ref, f"three-pass attention {t, hw, c}")
