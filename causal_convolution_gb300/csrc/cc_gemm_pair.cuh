@@ -1,9 +1,9 @@
 // The same implicit GEMM on CTA pairs: one tcgen05.mma.cta_group::2 computes
 // a 256 x BN tile across two SMs. CTA rank r of the pair streams its own A
 // tile (rows 128r .. 128r+127 of the pair tile) and its half of B (BN/2 rows)
-// into its own shared memory; the even CTA's single MMA thread reads both
-// CTAs' operands and writes each CTA's 128 accumulator rows into that CTA's
-// TMEM. Per k-block each SM now loads 16 KB of A and 16 KB of B for a 128 x BN
+// into its own shared memory; the MMAs that the even CTA's MMA warp issues
+// (from one elected lane) read both CTAs' operands and write each CTA's 128
+// accumulator rows into that CTA's TMEM. Per k-block each SM now loads 16 KB of A and 16 KB of B for a 128 x BN
 // share of the tile (the single-CTA kernel loads 16 KB + 32 KB), which lowers
 // both the L2 traffic and the shared-memory reads per MMA.
 //
@@ -59,7 +59,7 @@ __device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, in
 template <int AMODE>
 __device__ __forceinline__ int tile_first_tap(const GemmArgs& a, int batch, int mp) {
   if (AMODE != kAIm2col || a.lo_d >= 0) return 0;
-  // 32-bit arithmetic (m_total < 2^31 - 1024): the MMA thread runs this
+  // 32-bit arithmetic (m_total < 2^31 - 1024): the MMA warp runs this
   // between two tiles, where 64-bit divisions showed up as idle tensor cycles
   const unsigned plane = static_cast<unsigned>(a.img_h) * a.img_w;
   const unsigned per_image = plane * a.img_d;
