@@ -70,6 +70,14 @@ def test_noalloc_head_matches_workspace_head_on_two_calls():
     assert np.isfinite(to_np(got1)).all()
 
 
+def test_noalloc_head_near_its_scratch_limit():
+    # 547 x 547 = 299,209 positions: 384 below the 299,593 the scratch holds
+    max_positions = api.HEAD_NOALLOC_SCRATCH_BYTES // (api.HEAD_G_CH * 2)
+    assert max_positions - 384 == 547 * 547
+    got, ref, _, _ = both_entry_points(1, 1, 547, 547, 64, seed=53)
+    assert_same_bits(got, ref, "noalloc head at 299,209 positions")
+
+
 def test_noalloc_head_rejects_more_than_its_scratch_holds():
     max_positions = api.HEAD_NOALLOC_SCRATCH_BYTES // (api.HEAD_G_CH * 2)
     w = 512
