@@ -166,7 +166,9 @@ size_t cc_attn_workspace_bytes(int t, int hw);
 /* S[f,i,j] = sum_c q[f,i,c] k[f,j,c] in fp32 (unscaled). q, k: T frames of HW
  * rows with row strides ld_q, ld_k elements (frame stride HW*ld); s: row
  * stride ld_s floats. Needs C % 64 == 0, ld_q and ld_k % 8 == 0,
- * ld_s % 4 == 0, ld_s >= HW. */
+ * ld_s % 4 == 0, ld_s >= HW. S leaves through TMA tensor stores, which end
+ * each row on a 16-byte boundary: when HW % 4 != 0, columns HW .. (the next
+ * multiple of 4) - 1 may be written (with zeros); nothing past them is. */
 cc_status cc_attn_scores(const cc_bf16* q, const cc_bf16* k, float* s, int t, int hw, int c, int64_t ld_q,
                          int64_t ld_k, int64_t ld_s, void* stream);
 
@@ -215,9 +217,13 @@ int cc_attn_exp_key_tiles(int hw);
 size_t cc_attn_exp_workspace_bytes(int t, int hw);
 
 /* Step 1 from q, k [T, HW, C] (row strides ld_q, ld_k elements). e: row
- * stride ld_e elements (ld_e >= HW, % 8 == 0; keys HW .. ld_e-1 are not
- * written); stats: T*HW*cc_attn_exp_key_tiles(HW) pairs (c_t, l_t),
- * row-major [T][HW][tiles]. Needs C % 64 == 0, scale finite and > 0. */
+ * stride ld_e elements (ld_e >= HW, % 8 == 0); keys HW .. ld_e-1 are not
+ * written when e is 32-byte aligned and ld_e % 16 == 0 (E leaves from
+ * registers in 32-byte pieces), otherwise E leaves through TMA tensor stores,
+ * which end each row on a 16-byte boundary and may write keys HW .. (the next
+ * multiple of 8) - 1 with zeros, nothing past them; stats:
+ * T*HW*cc_attn_exp_key_tiles(HW) pairs (c_t, l_t), row-major [T][HW][tiles].
+ * Needs C % 64 == 0, scale finite and > 0. */
 cc_status cc_attn_scores_exp(const cc_bf16* q, const cc_bf16* k, cc_bf16* e, float* stats, int t, int hw, int c,
                              int64_t ld_q, int64_t ld_k, int64_t ld_e, float scale, void* stream);
 
