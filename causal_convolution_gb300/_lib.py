@@ -57,6 +57,7 @@ SIGNATURES = {
     "cc_copy_to_host": (_I, [_P, _P, _Z, _I, _P]),
     "cc_debug_im2col_tile": (_I, [_P, _P] + [_I] * 19 + [_P]),
     "cc_debug_wait_timeout": (_I, [_L, _P]),
+    "cc_debug_conv_bad_tile_order": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
 }
 
 _lib = None

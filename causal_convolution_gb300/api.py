@@ -25,7 +25,7 @@ __all__ = [
     "cc_head_prepare", "cc_head_workspace_bytes", "cc_head_temporal", "cc_head_stencil", "cc_head_out",
     "cc_attn_scores_stats", "cc_attn_fused_workspace_bytes", "cc_attn_frame_fused",
     "cc_head_out_fused", "cc_head_out_noalloc", "HEAD_NOALLOC_SCRATCH_BYTES", "cc_copy_to_host",
-    "cc_debug_im2col_tile", "cc_debug_wait_timeout",
+    "cc_debug_im2col_tile", "cc_debug_wait_timeout", "cc_debug_conv_bad_tile_order",
     "HEAD_COUT", "HEAD_G_CH",
 ]
 
@@ -409,3 +409,12 @@ def cc_debug_im2col_tile(x, tile, lower, upper, c0, start, offsets, stream=None)
 
 def cc_debug_wait_timeout(limit_ns: int, stream=None) -> None:
     _check(_lib.load().cc_debug_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def cc_debug_conv_bad_tile_order(x, wp, y, entry: int, stream=None) -> None:
+    n, d, h, w, cout = y.shape
+    cin = x.shape[-1]
+    if tuple(x.shape) != (n, d, h, w, cin) or wp.numel() != 27 * cout * cin:
+        raise ValueError("debug_conv_bad_tile_order: x must be [N,D,H,W,Cin] of y and wp hold 27*Cout*Cin elements")
+    _check(_lib.load().cc_debug_conv_bad_tile_order(_ptr(x, name="x"), _ptr(wp, name="wp"), _ptr(y, name="y"), n, d,
+                                                    h, w, cin, cout, int(entry), _stream(stream)))

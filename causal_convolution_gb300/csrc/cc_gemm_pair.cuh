@@ -36,19 +36,25 @@ struct PairShape {
 };
 
 // tile -> (batch, pair row tile, column tile); the CTA of rank r takes row
-// tile 2 * mp + r.
-__device__ __forceinline__ void pair_decode_tile(const GemmArgs& a, int tile, int& batch, int& mp, int& nt) {
+// tile 2 * mp + r. False when the host-made row-tile order maps the tile
+// outside the pair row tiles: every role then skips the tile, and the
+// producers record DEVERR_BOUNDS (CC_ERR_DEVICE at the next device check).
+__device__ __forceinline__ bool pair_decode_tile(const GemmArgs& a, int tile, int& batch, int& mp, int& nt) {
+  const int mpt = (a.m_tiles + 1) / 2;
   nt = tile % a.n_tiles;
   const int r = tile / a.n_tiles;
   if (a.batch_outer) {
-    const int mpt = (a.m_tiles + 1) / 2;
     mp = r % mpt;
     batch = r / mpt;
   } else {
     batch = r % a.batches;
     mp = r / a.batches;
   }
-  if (a.mp_perm_n > 0) mp = a.mp_perm[mp];
+  if (a.mp_perm_n > 0) {
+    if (mp >= a.mp_perm_n) return false;
+    mp = a.mp_perm[mp];
+  }
+  return mp < mpt;
 }
 
 // Taps are ordered by their temporal offset. With zero frames before frame 0
@@ -156,7 +162,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int k = 0, tile; ok && (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
         if (tile < 0) continue;
         int batch, mp, nt;
-        pair_decode_tile(args, tile, batch, mp, nt);
+        if (!pair_decode_tile(args, tile, batch, mp, nt)) {
+          atomicOr(args.err, DEVERR_BOUNDS);
+          continue;
+        }
         const int m0 = (2 * mp + static_cast<int>(rank)) * kBlockM;
         const int nb0 = nt * BN + static_cast<int>(rank) * S::kHalfN;  // this CTA's half of the columns
         int cw = 0, ch = 0, cd = 0, cn = 0;
@@ -231,7 +240,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int k = 0, tile; ok && (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
         if (tile < 0) continue;
         int batch, mp, nt;
-        pair_decode_tile(args, tile, batch, mp, nt);
+        if (!pair_decode_tile(args, tile, batch, mp, nt)) continue;
         const int kb0 = tile_first_tap<AMODE>(args, batch, mp) * args.kb_per_tap;
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, args.err, tlim))) {
           ok = false;
@@ -291,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     for (int k = 0, tile; (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
       if (tile < 0) continue;
       int batch, mp, nt;
-      pair_decode_tile(args, tile, batch, mp, nt);
+      if (!pair_decode_tile(args, tile, batch, mp, nt)) continue;
       if (!named_barrier_and(1, 128, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
       tc_fence_after();
       const int m0 = (2 * mp + static_cast<int>(rank)) * kBlockM;
@@ -422,7 +431,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     for (int k = 0, tile; (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
       if (tile < 0) continue;
       int batch, mp, nt;
-      pair_decode_tile(args, tile, batch, mp, nt);
+      if (!pair_decode_tile(args, tile, batch, mp, nt)) continue;
       if (!named_barrier_and(1, 128, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
       tc_fence_after();
       const int m0 = (2 * mp + static_cast<int>(rank)) * kBlockM;
@@ -491,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     for (int k = 0, tile; (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
       if (tile < 0) continue;
       int batch, mp, nt;
-      pair_decode_tile(args, tile, batch, mp, nt);
+      if (!pair_decode_tile(args, tile, batch, mp, nt)) continue;
       // uniform over the four epilogue warps (shared named barriers below)
       if (!named_barrier_and(1, 128, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
       tc_fence_after();
@@ -538,7 +547,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     for (int k = 0, tile; (tile = pair_tile(args, pair, npairs, k)) < args.num_tiles; ++k) {
       if (tile < 0) continue;
       int batch, mp, nt;
-      pair_decode_tile(args, tile, batch, mp, nt);
+      if (!pair_decode_tile(args, tile, batch, mp, nt)) continue;
       // warp-uniform: the lanes leave together (they share .sync.aligned ops)
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, args.err, tlim))) break;
       tc_fence_after();

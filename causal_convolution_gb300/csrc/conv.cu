@@ -118,9 +118,13 @@ extern "C" cc_status cc_conv3d_prepare(const cc_bf16* w, cc_bf16* wp, int cout, 
   return launch_status("conv3d_prepare");
 }
 
-extern "C" cc_status cc_conv3d_causal(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* y, int n,
-                                      int d, int h, int w, int cin, int cout, int hist, void* stream) {
-  const char* what = "conv3d_causal";
+namespace cc {
+namespace {
+
+// The causal conv; bad_entry >= 0 (self test only) replaces that entry of the
+// pair tiles' walking order by one past every row tile.
+cc_status conv3d_causal_impl(const char* what, const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* y,
+                             int n, int d, int h, int w, int cin, int cout, int hist, void* stream, int bad_entry) {
   cc_status st;
   if (empty_request(what, {n, d, h, w}, &st)) return st;
   if ((st = check_ptrs(what, {x, wp, y})) != CC_OK) return st;
@@ -169,11 +173,30 @@ extern "C" cc_status cc_conv3d_causal(const cc_bf16* x, const cc_bf16* wp, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pair) {
     set_frame_interleaved_order(a);
+    if (bad_entry >= 0) {
+      if (bad_entry >= a.mp_perm_n) return fail(CC_ERR_INVALID, "%s: no walking-order entry %d", what, bad_entry);
+      a.mp_perm[bad_entry] = 0xFFFF;
+    }
     if (bias) return launch_tc_gemm_pair<256, kAIm2col, false, false, true>(ta, tb, a, di, s, what);
     return launch_tc_gemm_pair<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
   }
+  if (bad_entry >= 0) return fail(CC_ERR_INVALID, "%s: one row tile has no walking order", what);
   if (bias) return launch_tc_gemm<256, kAIm2col, false, false, true>(ta, tb, a, di, s, what);
   return launch_tc_gemm<256, kAIm2col, false, false, false>(ta, tb, a, di, s, what);
+}
+
+}  // namespace
+}  // namespace cc
+
+extern "C" cc_status cc_conv3d_causal(const cc_bf16* x, const cc_bf16* wp, const cc_bf16* bias, cc_bf16* y, int n,
+                                      int d, int h, int w, int cin, int cout, int hist, void* stream) {
+  return conv3d_causal_impl("conv3d_causal", x, wp, bias, y, n, d, h, w, cin, cout, hist, stream, -1);
+}
+
+extern "C" cc_status cc_debug_conv_bad_tile_order(const cc_bf16* x, const cc_bf16* wp, cc_bf16* y, int n, int d,
+                                                  int h, int w, int cin, int cout, int entry, void* stream) {
+  if (entry < 0) return fail(CC_ERR_INVALID, "conv bad-order probe: entry must be >= 0");
+  return conv3d_causal_impl("conv bad-order probe", x, wp, nullptr, y, n, d, h, w, cin, cout, 0, stream, entry);
 }
 
 extern "C" cc_status cc_resample_prepare(const cc_bf16* w, cc_bf16* pw, int cout, int cin, void* stream) {

@@ -32,6 +32,19 @@ cc_status cc_debug_im2col_tile(const cc_bf16* x, cc_bf16* tile, int n, int d_in,
  * without hanging or faulting the GPU. */
 cc_status cc_debug_wait_timeout(int64_t limit_ns, void* stream);
 
+/* cc_conv3d_causal (no bias, zero history) with entry `entry` of the CTA
+ * pairs' walking order over the 256-row tiles replaced by a row tile that does
+ * not exist. The kernel's own check of the order finds it: that tile is
+ * skipped by every role (its 256 output rows are not written), the other
+ * tiles are computed as usual, and the device error word records an index
+ * failure, which the next cc_check_device() reports as CC_ERR_DEVICE. Needs a
+ * shape whose conv walks an explicit order (two or more frames, 2 to 512
+ * pair row tiles) and 0 <= entry < its pair row tiles; CC_ERR_INVALID
+ * otherwise. Tests that failure path without any
+ * out-of-range access. */
+cc_status cc_debug_conv_bad_tile_order(const cc_bf16* x, const cc_bf16* wp, cc_bf16* y, int n, int d, int h, int w,
+                                       int cin, int cout, int entry, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -481,6 +481,30 @@ def test_kernel_wait_timeout_is_reported_and_cleared():
     assert_parity(to_np(y), ref, "conv after a timeout")
 
 
+def test_bad_tile_order_is_reported_and_skipped():
+    # entry 0 of the pair tiles' walking order is the pair row tile 0 (rows
+    # 0-255: the zero-history tiles of frame 0 come first, in plain order);
+    # the self test replaces it by a row tile that does not exist
+    n, d, h, w, cin, cout = 1, 3, 16, 32, 64, 64
+    inp = inputs.conv_inputs(n, d, h, w, cin, cout, 41, device=DEV)
+    wp = empty(27 * cout * cin)
+    api.cc_conv3d_prepare(inp["w"], wp)
+    y = torch.full((n, d, h, w, cout), float("nan"), dtype=BF16, device=DEV)
+    api.cc_debug_conv_bad_tile_order(inp["x"], wp, y, 0)
+    with pytest.raises(api.CCError) as e:
+        api.cc_check_device()
+    assert e.value.status == 5
+    api.cc_check_device()  # the word was cleared; the context is still usable
+    rows = to_np(y).reshape(-1, cout)
+    assert np.isnan(rows[:256]).all(), "the skipped tile's rows were written"
+    ref = oracle.causal_conv3d(to_np(inp["x"]), to_np(inp["w"]), None).reshape(-1, cout)
+    assert_parity(rows[256:], ref[256:], "conv rows of the other tiles")
+    with pytest.raises(api.CCError) as e:
+        api.cc_debug_conv_bad_tile_order(inp["x"], wp, y, 6)  # 1536 rows: pair row tiles 0-5
+    assert e.value.status == 1
+    api.cc_check_device()
+
+
 # ------------------------------------------------------ fused resampler --
 
 def run_resample_fused(x, w, b, skip, hist=0):
