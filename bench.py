@@ -469,17 +469,19 @@ def oracle_sample_step(cpu, budget_s: float, rng, per_config=None):
 
     def timed(fn, total, batch):
         """Calls of `batch` sampled outputs until the stage's share of the
-        budget is spent (at least one); returns (points, seconds, ms per
-        chunk). The batch is fixed per stage, so the per-call setup is spread
-        over the same number of outputs whatever the budget."""
+        budget is spent (at least one) or the configuration's outputs are all
+        counted; returns (points, seconds, ms per chunk). The batch is fixed
+        per stage (the last call may be shorter), so the per-call setup is
+        spread over the same number of outputs whatever the budget."""
         npts, dt = 0, 0.0
         # until the stage's share of the budget is spent, or as many outputs
         # as the configuration has were timed
         while npts == 0 or (dt < per_stage and npts < total):
+            b = min(batch, total - npts)  # the last call stops at the configuration's count
             t0 = time.perf_counter()
-            fn(batch)
+            fn(b)
             dt += time.perf_counter() - t0
-            npts += batch
+            npts += b
         return npts, dt, dt / npts * total * 1e3
 
     stages = []
