@@ -732,3 +732,48 @@ def test_dependent_chain_on_one_stream_matches_synchronised_run():
     a, b = chain(False), chain(True)
     for name, u, v in zip(("conv", "resampler", "head"), a, b):
         assert torch.equal(u, v), f"{name}: the queued chain differs from the synchronised one"
+
+
+def test_two_streams_at_once_match_one_after_the_other():
+    # independent stages queued on two streams at the same time (their
+    # persistent kernels then share the SMs and the device error word) give
+    # the same bits as the same calls one after the other on one stream
+    g = torch.Generator(device=DEV).manual_seed(72)
+    n, d, h, w, c = 1, 3, 24, 40, 64
+    x = torch.randn((n, d, h, w, c), generator=g, device=DEV).to(BF16)
+    wc = (torch.randn((c, c, 3, 3, 3), generator=g, device=DEV) / (27 * c) ** 0.5).to(BF16)
+    bc = (torch.randn((c,), generator=g, device=DEV) * 0.1).to(BF16)
+    wr = (torch.randn((c, c, 3, 3, 3), generator=g, device=DEV) / (27 * c) ** 0.5).to(BF16)
+    skip = torch.randn((n, d, h, w, c), generator=g, device=DEV).to(BF16)
+    wh = (torch.randn((12, c, 3, 3, 3), generator=g, device=DEV) / (27 * c) ** 0.5).to(BF16)
+    bh = (torch.randn((12,), generator=g, device=DEV) * 0.1).to(BF16)
+    t, hw, ca = 2, 500, 128
+    q, k, v = (torch.randn((t, hw, ca), generator=g, device=DEV).to(BF16) for _ in range(3))
+    wpc = empty(27 * c * c)
+    api.cc_conv3d_prepare(wc, wpc)
+    pw = empty(48 * c * c)
+    api.cc_resample_prepare(wr, pw)
+    wph = empty(3 * api.HEAD_G_CH * c)
+    api.cc_head_prepare(wh, wph)
+    torch.cuda.synchronize()
+
+    def run(two_streams):
+        y = empty(n, d, h, w, c)
+        hd = empty(n, d, h, w, api.HEAD_COUT)
+        up = empty(n, d, 2 * h, 2 * w, c)
+        o = empty(t, hw, ca)
+        ws = torch.empty(api.cc_attn_exp_workspace_bytes(t, hw), dtype=torch.uint8, device=DEV)
+        sa = torch.cuda.Stream()
+        sb = torch.cuda.Stream() if two_streams else sa
+        api.cc_conv3d_causal(x, wpc, bc, y, stream=sa)
+        api.cc_attn_frame_exp(q, k, v, o, ws, stream=sb)
+        api.cc_head_out_fused(x, wph, bh, hd, stream=sa)
+        api.cc_resample_up2_fused(x, pw, bc, skip, up, stream=sb)
+        sa.synchronize()
+        sb.synchronize()
+        api.cc_check_device()
+        return y, o, hd, up
+
+    a, b = run(True), run(False)
+    for name, u, v in zip(("conv", "attention", "head", "resampler"), a, b):
+        assert torch.equal(u.view(torch.int16), v.view(torch.int16)), f"{name}: two streams differ from one"
